@@ -1,0 +1,46 @@
+"""Block-wise FP8 requantisation of updated parameters into the AllGather staging
+buffer (oracle; test infrastructure only).
+
+Sources: "veScale-FSDP: Flexible and High-Performance FSDP at Scale" (bud-325
+summary), TL;DR and Key claims: block-wise FP8 in the DeepSeek-V3 style, one
+scale per block; feynmanwiki walkthrough (paper sections 2-4): every quantisation
+block must live entirely on one device because its values share scale metadata,
+which is what RaggedShard's granularity guarantees.
+
+Readings (the pages give no formula): blocks are 128x128 tiles of the tensor's
+row-major 2-D view, clipped at the edges (1-D tensors: 1x128); per tile
+    amax = max |p'|,  s = amax / 448 (fp32 division),
+    code = e4m3(p' / s)  (fp32 division, then round-to-nearest-even, saturating),
+and an all-zero tile gets s = 0 with codes +0 / -0 following each element's sign.
+Codes go to the same local offsets as the parameters; s goes to the tile's slot.
+"""
+
+import numpy as np
+
+from .codecs import e4m3_encode
+from .planner import fp8_tiles
+
+F32 = np.float32
+
+
+def fp8_tile(p):
+    """One tile -> (uint8 E4M3 codes, fp32 scale)."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    amax = np.max(np.abs(p)) if p.size else F32(0)
+    if amax == 0:
+        return e4m3_encode(p), F32(0)  # +-0 -> 0x00 / 0x80
+    s = F32(amax) / F32(448)
+    return e4m3_encode(p / s), F32(s)
+
+
+def quant_fp8(layout, dev_lo, dev_hi, master, fp8_out, fp8_scale, tiles=None):
+    """Requantise every FP8 tile of local shards [dev_lo, dev_hi) (or the given
+    subset).  Returns updated copies (fp8_out, fp8_scale); bytes outside tiles are
+    left as they were."""
+    fp8_out, fp8_scale = fp8_out.copy(), fp8_scale.copy()
+    it = fp8_tiles(layout, dev_lo, dev_hi) if tiles is None else tiles
+    for slot, pos in it:
+        q, s = fp8_tile(master[pos])
+        fp8_out[pos] = q
+        fp8_scale[slot] = s
+    return fp8_out, fp8_scale
