@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 DBuffer step (one JSON line on rank 0).
+
+One step = the hot path over one batch of synthetic input:
+  * the DBuffer step of one Llama-3-8B-shaped decoder layer held in one DBuffer
+    of V = 8 simulated devices (all 8 local shards, 218.1 M parameters):
+    bq_pack (fused pre-communication copy/scale/zero into the bf16 gradient
+    buffer) then bq_step_adam8 (block-wise 8-bit Adam fused with 128x128 FP8
+    requantisation into the AllGather staging buffer);
+  * Muon's Newton-Schulz (5 iterations) on the batch of whole matrices
+    4096x4096, 4096x14336, 14336x4096 (when --muon is on).
+value = algorithmic DBuffer bytes per step / DBuffer time per step (GB/s);
+the Muon part is reported beside it in TFLOP/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): one rank per GPU, each processes its own layer (weak
+scaling, no collective on the data path); value sums the ranks' bytes over the
+slowest rank's time.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "DBuffer step GB/s & fraction of HBM peak; Muon NS TFLOP/s (1 GB300)"
+WORKLOAD = "llama3-8b-layer"
+MUON = "muon-ns"
+L2_BYTES = 126 * 2 ** 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------- algorithmic bytes
+
+def step_bytes(table, dev_lo, dev_hi):
+    """Algorithmic DRAM bytes of one DBuffer step over local shards [dev_lo, dev_hi).
+    pack: read bf16 grad 2 + write bf16 DBuffer 2 per element, +2 per padding
+    element (zeroed); adam8 + FP8: grad 2 + master 4+4 + m 1+1 + v 1+1 + fp8 1
+    = 15 per element, + 16 B per Adam block (two fp32 scales read and written)
+    + 4 B per FP8 tile (scale written)."""
+    iv = table.dev_intervals(dev_lo, dev_hi)
+    elems = int(iv[:, 3].sum())
+    total = (dev_hi - dev_lo) * table.S
+    pads = total - elems
+    m0, m1 = table.slot_range(dev_lo, dev_hi)
+    f0, f1 = table.slot_range(dev_lo, dev_hi, fp8=True)
+    fp8_elems = 0
+    for k, i, t_off, ln, loff, ms, fs in iv:
+        if fs >= 0:
+            fp8_elems += int(ln)
+    pack = 4 * elems + 2 * pads
+    adam = 14 * elems + fp8_elems + 16 * (m1 - m0) + 4 * (f1 - f0)
+    return dict(elems=elems, pads=pads, pack=pack, adam=adam, total=pack + adam,
+                adam_blocks=m1 - m0, fp8_tiles=f1 - f0)
+
+
+def adam_launches(table, dev_lo, dev_hi):
+    """Kernels one bq_step_adam8 call launches (one per non-empty group kind)."""
+    kinds = set()
+    for k, i, t_off, ln, loff, ms, fs in table.dev_intervals(dev_lo, dev_hi):
+        _, _, rows, cols, g, kind, fp8 = table.tensors[i]
+        if kind == W.ADAM_FLAT256 and (rows == 1 or not fp8):
+            kinds.add("flat256")
+        elif kind == W.ADAM_TILE128 and rows == 1:
+            kinds.add("flat128")
+        elif kind == W.ADAM_TILE128:
+            kinds.add("tile")
+        else:
+            kinds.add("strip")
+    return len(kinds)
+
+
+def muon_flops(shapes, steps=5):
+    """Nominal FLOPs of the iteration: per step X X^T (2 m^2 n), A A (2 m^3),
+    B X (2 m^2 n), m = min dim, n = max dim."""
+    tot = 0
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        tot += steps * (4 * m * m * n + 2 * m ** 3)
+    return tot
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            self.path = os.path.join("/tmp", f"bq_clocks_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class DBufferStep:
+    """Device-resident buffers of one unit's DBuffer step (all V local shards)."""
+
+    def __init__(self, cfg, dev, seed):
+        import torch
+
+        import block_quant_gb300 as bq
+
+        self.bq, self.torch, self.dev = bq, torch, dev
+        unit = cfg.units[0]
+        self.V, self.lo, self.hi = cfg.V, cfg.dev_lo, cfg.dev_hi
+        self.layout = bq.plan(unit.tensors, cfg.V, cfg.alpha, cfg.start_align)
+        self.table = W.Table(self.layout.export())
+        S = self.table.S
+        n = (self.hi - self.lo) * S
+        self.n = n
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        m0, m1 = self.table.slot_range(self.lo, self.hi)
+        f0, f1 = self.table.slot_range(self.lo, self.hi, fp8=True)
+        self.ws = torch.empty(self.layout.upload_bytes(self.lo, self.hi), dtype=torch.uint8, device=dev)
+        self.shard = self.layout.upload(self.lo, self.hi, self.ws)
+        # synthetic inputs with the recipe's distributions, drawn on the device
+        self.master = torch.randn(n, generator=g, device=dev) * 0.02
+        self.m = torch.randint(-127, 128, (n,), generator=g, device=dev, dtype=torch.int8)
+        self.v = torch.randint(64, 256, (n,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        self.ms = (torch.rand(m1 - m0, generator=g, device=dev) + 0.5) * (1e-3 / 127)
+        self.vs = (torch.rand(m1 - m0, generator=g, device=dev) + 0.5) * (1e-6 / 255)
+        self.dbuf = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        self.fp8 = torch.zeros(n, dtype=torch.uint8, device=dev)
+        self.fs = torch.zeros(max(f1 - f0, 1), dtype=torch.float32, device=dev)
+        # per-tensor gradients over the owned ranges (distinct allocations)
+        self.grads, self.host_grads, ptrs = {}, {}, np.zeros(len(unit.tensors), np.int64)
+        for i in range(len(unit.tensors)):
+            a, b = self.table.owned_range(i, self.lo, self.hi)
+            if b > a:
+                gr = (torch.randn(b - a, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+                self.grads[i] = gr
+                ptrs[i] = gr.data_ptr() - 2 * a
+        self.gptrs = torch.from_numpy(ptrs).to(dev)
+        self.hp = bq.adam_hparams(cfg.lr, cfg.b1, cfg.b2, cfg.eps, cfg.t)
+        self.bytes = step_bytes(self.table, self.lo, self.hi)
+        self.launches = 1 + adam_launches(self.table, self.lo, self.hi)
+        torch.cuda.synchronize(dev)
+
+    def pack(self, stream):
+        self.bq.pack(self.shard, self.gptrs, self.dbuf, 1.0 / self.V, False, stream=stream)
+
+    def adam(self, stream):
+        self.bq.step_adam8(self.shard, self.dbuf, self.master, self.m, self.v, self.ms, self.vs, self.hp,
+                           self.fp8, self.fs, stream=stream)
+
+    def pin_host(self):
+        torch = self.torch
+        self.host_grads = {i: torch.empty(g.numel(), dtype=torch.bfloat16, pin_memory=True) for i, g in self.grads.items()}
+        for i, g in self.grads.items():
+            self.host_grads[i].copy_(g)
+        self.host_fp8 = torch.empty(self.fp8.numel(), dtype=torch.uint8, pin_memory=True)
+        self.host_fs = torch.empty(self.fs.numel(), dtype=torch.float32, pin_memory=True)
+        self.h2d = sum(g.numel() * 2 for g in self.grads.values())
+        self.d2h = self.fp8.numel() + self.fs.numel() * 4
+
+
+class MuonBatch:
+    def __init__(self, shapes, dev, seed):
+        import torch
+
+        import block_quant_gb300 as bq
+
+        self.bq = bq
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.xs = [(torch.randn(r, c, generator=g, device=dev) * 1e-3).to(torch.bfloat16) for r, c in shapes]
+        self.ys = [torch.empty_like(x) for x in self.xs]
+        self.mats = [(x, y, r, c) for (x, y, (r, c)) in zip(self.xs, self.ys, shapes)]
+        self.ws = torch.empty(bq.muon_ns_workspace(self.mats), dtype=torch.uint8, device=dev)
+        self.flops = muon_flops(shapes)
+        self.launches = None
+
+    def run(self, stream):
+        self.bq.muon_ns(self.mats, self.ws, stream=stream)
+
+
+def cpu_baseline(seconds=12.0):
+    """The oracle, as it stands, on a bounded sample of the same workload: whole
+    128-row x 256-column strips of the Llama-3-8B layer's 2-D tensors (pack
+    arithmetic, the 128 Adam blocks and the two FP8 tiles of each strip), timed
+    on one host core.  Returns GB/s at the same algorithmic bytes per element."""
+    from oracle import adam8 as OA
+    from oracle import codecs as OC
+    from oracle import fp8 as OF
+
+    cfg = W.config(WORKLOAD)
+    hp = OA.adam_hparams(cfg.lr, cfg.b1, cfg.b2, cfg.eps, cfg.t)
+    rng = np.random.default_rng(0)
+    elems, spent, strips = 0, 0.0, 0
+    sc = np.float32(1.0 / cfg.V)
+    while spent < seconds:
+        g = (rng.standard_normal((128, 256)) * 1e-3).astype(np.float32)
+        gb = OC.f32_to_bf16_bits(g)
+        p = (rng.standard_normal((128, 256)) * 0.02).astype(np.float32)
+        qm = rng.integers(-127, 128, (128, 256)).astype(np.int8)
+        qv = rng.integers(64, 256, (128, 256)).astype(np.uint8)
+        t0 = time.perf_counter()
+        packed = OC.f32_to_bf16_bits(OC.bf16_bits_to_f32(gb) * sc)
+        p1 = np.empty_like(p)
+        for r in range(128):
+            p1[r], _, _, _, _ = OA.adam8_block(packed[r], p[r], qm[r], qv[r], np.float32(1e-5), np.float32(4e-9), hp)
+        OF.fp8_tile(p1[:, :128])
+        OF.fp8_tile(p1[:, 128:])
+        spent += time.perf_counter() - t0
+        elems += 128 * 256
+        strips += 1
+    bpe = 19.0 + 16.0 / 256 + 4.0 / 16384
+    return dict(value=elems * bpe / spent / 1e9, unit="GB/s", cores=1, kind="oracle",
+                sample=f"{strips} strips of 128x256 elements ({elems} elements) of the llama3-8b layer: "
+                       f"oracle pack + 8-bit Adam + FP8, numpy, one thread, {spent:.1f} s")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    import block_quant_gb300 as bq
+
+    bq.load()
+    cfg = W.config(WORKLOAD)
+    step = DBufferStep(cfg, dev, seed=1000 + rank)
+    muon = MuonBatch(W.config(MUON).muon_shapes, dev, seed=2000 + rank) if args.muon else None
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        step.pack(stream)
+        if ev:
+            ev[1].record(stream)
+        step.adam(stream)
+        if ev:
+            ev[2].record(stream)
+        if muon:
+            muon.run(stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        one_step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    pack_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    adam_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    muon_ms = [e[2].elapsed_time(e[3]) for e in evs] if muon else [0.0]
+    dbuf_ms = statistics.mean(p + a for p, a in zip(pack_ms, adam_ms))
+
+    # end to end through the public API: H2D of the step's gradients from pinned
+    # host memory, the step, D2H of the FP8 staging buffer and its scales
+    step.pin_host()
+    for _ in range(2):
+        for i, g in step.grads.items():
+            g.copy_(step.host_grads[i], non_blocking=True)
+        one_step()
+        step.host_fp8.copy_(step.fp8, non_blocking=True)
+        step.host_fs.copy_(step.fs, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    ke = max(10, args.steps // 4)
+    e0.record(stream)
+    for _ in range(ke):
+        for i, g in step.grads.items():
+            g.copy_(step.host_grads[i], non_blocking=True)
+        one_step()
+        step.host_fp8.copy_(step.fp8, non_blocking=True)
+        step.host_fs.copy_(step.fs, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / ke
+
+    local_vals = torch.tensor([total_ms / args.steps, dbuf_ms, statistics.mean(muon_ms), e2e_ms],
+                              dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(local_vals, op=dist.ReduceOp.MAX)
+    ms_step, dbuf_ms_max, muon_ms_max, e2e_max = local_vals.tolist()
+    if rank == 0:
+        pk = peaks()
+        B = step.bytes["total"]
+        value = world * B / (dbuf_ms_max * 1e-3) / 1e9
+        adam_mean = statistics.mean(adam_ms)
+        adam_gbs = step.bytes["adam"] / (adam_mean * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {
+                "workload": "llama3-8b-layer DBuffer step (V=8, all 8 local shards) + Muon NS batch "
+                            "[4096x4096, 4096x14336, 14336x4096] x 5 iterations" if muon else
+                            "llama3-8b-layer DBuffer step (V=8, all 8 local shards)",
+                "elements": step.bytes["elems"], "padding_elements": step.bytes["pads"], "S": step.table.S,
+                "bytes_per_step": B, "l2": f"inputs {step.n * 13 / 1e9:.1f} GB > L2: no flush needed",
+                "parallelism": f"dp{world}: one independent layer per GPU, no data-path collective",
+            },
+            "hbm_frac": round(value / world / pk["hbm"], 4),
+            "dbuffer_ms": round(dbuf_ms_max, 4),
+            "pack": {"ms": round(statistics.mean(pack_ms), 4),
+                     "GB/s": round(step.bytes["pack"] / (statistics.mean(pack_ms) * 1e-3) / 1e9, 1)},
+            "roofline": {"bound": "hbm", "kernel": "bq_step_adam8 (8-bit Adam + fused FP8)",
+                         "achieved": round(adam_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": round(adam_gbs / pk["hbm"], 4), "traffic": None,
+                         "peak_source": f"{pk['src']} hbm_gbs (STREAM-style copy)",
+                         "ms": round(adam_mean, 4), "algorithmic_bytes": step.bytes["adam"]},
+            "e2e": {"value": round(world * B / (e2e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": step.h2d, "d2h_bytes_per_step": step.d2h,
+                    "ms_per_step": round(e2e_max, 4)},
+            "gpu_launches": args.steps * (step.launches + (muon_launches(muon) if muon else 0)),
+            "clocks": clk,
+        }
+        if muon:
+            tf = world * muon.flops / (muon_ms_max * 1e-3) / 1e12
+            line["muon"] = {"value": round(tf, 1), "unit": "TFLOP/s", "ms": round(muon_ms_max, 3),
+                            "flops": muon.flops, "frac": round(tf / world / pk["bf16_sus"], 4),
+                            "peak": pk["bf16_sus"], "peak_source": f"{pk['src']} bf16_tflops_sustained"}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def muon_launches(muon):
+    return muon.bq.muon_launch_count(muon.mats) if hasattr(muon.bq, "muon_launch_count") else 0
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores, same
+    metric and unit, a bounded sample of the workload per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    per_step = []
+    for _ in range(args.warmup):
+        cpu_baseline(seconds=0.5)
+    for _ in range(args.steps):
+        per_step.append(cpu_baseline(seconds=1.0))
+    vals = [x["value"] for x in per_step]
+    v = statistics.mean(vals)
+    line = {
+        "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "llama3-8b-layer DBuffer step (V=8), bounded sample per step",
+                   "parallelism": "host, one core"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": per_step[0]["sample"].split(":")[0] + " per step (about 1 s of CPU work)"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--muon", dest="muon", action="store_true", default=True)
+    ap.add_argument("--no-muon", dest="muon", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+// C ABI of libbq: errors, device-table upload, argument validation and dispatch
+// to the step kernels.  All compute runs in the CUDA kernels; this file only
+// checks arguments, builds integer work tables and launches.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "bq_internal.h"
+
+namespace bq {
+
+static thread_local std::string g_last_error;
+
+int set_error(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+}  // namespace bq
+
+using namespace bq;
+
+struct bq_shard {
+  const bq_layout* layout;
+  int dev_lo, dev_hi;
+  int64_t total;  // elements of the shard range
+  DevTables dev;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsPlan {
+  size_t off_pieces, off_chunks, off_f256, off_f128, off_strips, off_tiles, bytes;
+};
+
+WsPlan ws_plan(const ShardTables& T) {
+  WsPlan p;
+  size_t o = 0;
+  p.off_pieces = o;
+  o = align_up(o + T.pieces.size() * sizeof(PackPiece), 256);
+  p.off_chunks = o;
+  o = align_up(o + T.chunk_first.size() * sizeof(int32_t), 256);
+  p.off_f256 = o;
+  o = align_up(o + T.flat256.size() * sizeof(FlatGroup), 256);
+  p.off_f128 = o;
+  o = align_up(o + T.flat128.size() * sizeof(FlatGroup), 256);
+  p.off_strips = o;
+  o = align_up(o + T.strips.size() * sizeof(RegionGroup), 256);
+  p.off_tiles = o;
+  o = align_up(o + T.tiles.size() * sizeof(RegionGroup), 256);
+  p.bytes = std::max<size_t>(o, 256);
+  return p;
+}
+
+int check_range(const bq_layout* L, int dev_lo, int dev_hi) {
+  if (!L) return set_error(BQ_EINVAL, "layout is NULL");
+  if (dev_lo < 0 || dev_hi > L->V || dev_lo >= dev_hi)
+    return set_error(BQ_EINVAL, "need 0 <= dev_lo < dev_hi <= V");
+  for (int64_t k = L->dev_first[dev_lo]; k < L->dev_first[dev_hi]; ++k)
+    if (L->intervals[k].local_off % 8)
+      return set_error(BQ_EALIGN, "interval local offsets must be multiples of 8 elements (plan with start_align % 8 == 0)");
+  if (int64_t(dev_hi - dev_lo) * L->S > (int64_t(1) << 40))
+    return set_error(BQ_EINVAL, "shard range too large");
+  return BQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bq_strerror(int code) {
+  switch (code) {
+    case BQ_OK: return "ok";
+    case BQ_EINVAL: return "invalid argument";
+    case BQ_EINFEASIBLE: return "no feasible layout";
+    case BQ_EALIGN: return "misaligned pointer or offset";
+    case BQ_ECUDA: return "CUDA error";
+    case BQ_ENOSPC: return "buffer or workspace too small";
+    case BQ_EDEVICE: return "no usable device";
+    default: return "unknown error";
+  }
+}
+
+const char* bq_last_error(void) { return g_last_error.c_str(); }
+
+int bq_version(void) { return 1; }
+
+int bq_layout_upload_bytes(const bq_layout* L, int dev_lo, int dev_hi, size_t* bytes) {
+  if (!bytes) return set_error(BQ_EINVAL, "bq_layout_upload_bytes: bytes is NULL");
+  if (int rc = check_range(L, dev_lo, dev_hi)) return rc;
+  ShardTables T;
+  build_shard_tables(*L, dev_lo, dev_hi, T);
+  const std::string bad = validate_shard_tables(*L, dev_lo, dev_hi, T);
+  if (!bad.empty()) return set_error(BQ_EINVAL, "bq_layout_upload_bytes: internal table check failed: " + bad);
+  *bytes = ws_plan(T).bytes;
+  return BQ_OK;
+}
+
+int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, size_t ws_bytes, bq_stream_t stream,
+                     bq_shard** out) {
+  if (!out) return set_error(BQ_EINVAL, "bq_layout_upload: out is NULL");
+  *out = nullptr;
+  if (int rc = check_range(L, dev_lo, dev_hi)) return rc;
+  if (!dev_ws || !aligned16(dev_ws)) return set_error(BQ_EALIGN, "bq_layout_upload: workspace NULL or misaligned");
+  ShardTables T;
+  build_shard_tables(*L, dev_lo, dev_hi, T);
+  const std::string bad = validate_shard_tables(*L, dev_lo, dev_hi, T);
+  if (!bad.empty()) return set_error(BQ_EINVAL, "bq_layout_upload: internal table check failed: " + bad);
+  const WsPlan p = ws_plan(T);
+  if (ws_bytes < p.bytes) return set_error(BQ_ENOSPC, "bq_layout_upload: workspace too small");
+  // stage everything in one host image, one copy, synchronised so the host image
+  // may be freed on return
+  std::vector<unsigned char> img(p.bytes, 0);
+  auto put = [&](size_t off, const void* src, size_t n) {
+    if (n) std::memcpy(img.data() + off, src, n);
+  };
+  put(p.off_pieces, T.pieces.data(), T.pieces.size() * sizeof(PackPiece));
+  put(p.off_chunks, T.chunk_first.data(), T.chunk_first.size() * sizeof(int32_t));
+  put(p.off_f256, T.flat256.data(), T.flat256.size() * sizeof(FlatGroup));
+  put(p.off_f128, T.flat128.data(), T.flat128.size() * sizeof(FlatGroup));
+  put(p.off_strips, T.strips.data(), T.strips.size() * sizeof(RegionGroup));
+  put(p.off_tiles, T.tiles.data(), T.tiles.size() * sizeof(RegionGroup));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(dev_ws, img.data(), p.bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string("bq_layout_upload: ") + cudaGetErrorString(e));
+
+  auto* sh = new bq_shard();
+  sh->layout = L;
+  sh->dev_lo = dev_lo;
+  sh->dev_hi = dev_hi;
+  sh->total = int64_t(dev_hi - dev_lo) * L->S;
+  auto* base = static_cast<unsigned char*>(dev_ws);
+  sh->dev.pieces = reinterpret_cast<const PackPiece*>(base + p.off_pieces);
+  sh->dev.chunk_first = reinterpret_cast<const int32_t*>(base + p.off_chunks);
+  sh->dev.flat256 = reinterpret_cast<const FlatGroup*>(base + p.off_f256);
+  sh->dev.flat128 = reinterpret_cast<const FlatGroup*>(base + p.off_f128);
+  sh->dev.strips = reinterpret_cast<const RegionGroup*>(base + p.off_strips);
+  sh->dev.tiles = reinterpret_cast<const RegionGroup*>(base + p.off_tiles);
+  sh->dev.nchunks = T.nchunks;
+  sh->dev.n_flat256 = int32_t(T.flat256.size());
+  sh->dev.n_flat128 = int32_t(T.flat128.size());
+  sh->dev.n_strips = int32_t(T.strips.size());
+  sh->dev.n_tiles = int32_t(T.tiles.size());
+  sh->dev.max_strip_tiles = T.max_strip_tiles;
+  *out = sh;
+  return BQ_OK;
+}
+
+void bq_shard_free(bq_shard* shard) { delete shard; }
+
+int bq_pack(const bq_shard* sh, const void* const* grad_ptrs, void* dbuf_grad, float scale, int accumulate,
+            bq_stream_t stream) {
+  if (!sh || !grad_ptrs || !dbuf_grad) return set_error(BQ_EINVAL, "bq_pack: NULL argument");
+  if (!aligned16(grad_ptrs) && (reinterpret_cast<uintptr_t>(grad_ptrs) & 7))
+    return set_error(BQ_EALIGN, "bq_pack: grad_ptrs must be 8-byte aligned");
+  if (!aligned16(dbuf_grad)) return set_error(BQ_EALIGN, "bq_pack: dbuf_grad must be 16-byte aligned");
+  return launch_pack(sh->dev, reinterpret_cast<const uint16_t* const*>(grad_ptrs),
+                     static_cast<uint16_t*>(dbuf_grad), sh->total, scale, accumulate ? 1 : 0, stream);
+}
+
+int bq_step_adam8(const bq_shard* sh, const void* grad, float* master, int8_t* m, uint8_t* v, float* m_scale,
+                  float* v_scale, const bq_adam_hp* hp, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream) {
+  if (!sh || !grad || !master || !m || !v || !m_scale || !v_scale || !hp)
+    return set_error(BQ_EINVAL, "bq_step_adam8: NULL argument");
+  if ((fp8_out == nullptr) != (fp8_scale == nullptr))
+    return set_error(BQ_EINVAL, "bq_step_adam8: fp8_out and fp8_scale must both be set or both NULL");
+  const void* ptrs[] = {grad, master, m, v, fp8_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return set_error(BQ_EALIGN, "bq_step_adam8: buffers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(m_scale) | reinterpret_cast<uintptr_t>(v_scale) |
+       reinterpret_cast<uintptr_t>(fp8_scale)) & 3)
+    return set_error(BQ_EALIGN, "bq_step_adam8: scale buffers must be 4-byte aligned");
+  AdamArgs a{static_cast<const uint16_t*>(grad), master, m, v, m_scale, v_scale, fp8_out, fp8_scale, *hp};
+  return launch_adam8(sh->dev, a, stream);
+}
+
+int bq_quant_fp8(const bq_shard* sh, const float* master, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream) {
+  if (!sh || !master || !fp8_out || !fp8_scale) return set_error(BQ_EINVAL, "bq_quant_fp8: NULL argument");
+  if (!aligned16(master) || !aligned16(fp8_out) || (reinterpret_cast<uintptr_t>(fp8_scale) & 3))
+    return set_error(BQ_EALIGN, "bq_quant_fp8: misaligned buffer");
+  return launch_quant_fp8(sh->dev, master, fp8_out, fp8_scale, stream);
+}
+
+int bq_muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes) { return muon_ns_workspace(batch, mats, bytes); }
+
+int bq_muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws,
+               size_t ws_bytes, bq_stream_t stream) {
+  return muon_ns(batch, mats, steps, a, b, c, eps, ws, ws_bytes, stream);
+}
+
+}  // extern "C"

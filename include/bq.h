@@ -1,0 +1,202 @@
+/*
+ * bq.h - C ABI of the GB300 DBuffer step (libbq.so).
+ *
+ * The library implements, for ONE GPU, the per-device hot path of veScale-FSDP
+ * ("veScale-FSDP: Flexible and High-Performance FSDP at Scale"): a RaggedShard
+ * layout planner that packs the tensors of one fully_shard unit into a DBuffer of
+ * V equal local shards, and the step over a device's shards of that buffer - the
+ * fused pre-communication pack of gradients, block-wise 8-bit Adam, block-wise FP8
+ * requantisation of the updated parameters - plus Muon's Newton-Schulz
+ * orthogonalisation of whole matrices.  V devices are simulated as layout only:
+ * the caller chooses which local shards [dev_lo, dev_hi) one call processes.
+ *
+ * Conventions (every entry point):
+ *   - returns int: BQ_OK (0) or a negative BQ_E* code; nothing aborts, traps or
+ *     throws across the ABI; bq_last_error() gives a message for the calling
+ *     thread's last failure.
+ *   - the CALLER owns every device buffer and stream; the library owns only the
+ *     host objects it returns (bq_layout, bq_shard) and frees them on *_free.
+ *   - device work is asynchronous on the given stream (a cudaStream_t passed as
+ *     bq_stream_t; NULL = legacy default stream); launch failures come back as
+ *     BQ_ECUDA.  Kernels do no device-wide synchronisation and no allocation.
+ *   - device pointers must be 16-byte aligned (BQ_EALIGN otherwise).
+ *   - element buffers of a shard range cover the global DBuffer offsets
+ *     [dev_lo*S, dev_hi*S): element at global offset x lives at index x - dev_lo*S.
+ *     Scale buffers cover the slots of devices [dev_lo, dev_hi): slot z lives at
+ *     index z - slot_base(dev_lo) (slot bases are in the exported table).
+ */
+#ifndef BQ_H
+#define BQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* bq_stream_t; /* == cudaStream_t */
+
+enum {
+  BQ_OK = 0,
+  BQ_EINVAL = -1,      /* bad argument or descriptor */
+  BQ_EINFEASIBLE = -2, /* no layout satisfies the constraints */
+  BQ_EALIGN = -3,      /* misaligned pointer, stride or layout offset */
+  BQ_ECUDA = -4,       /* CUDA runtime / launch error */
+  BQ_ENOSPC = -5,      /* caller buffer or workspace too small */
+  BQ_EDEVICE = -6      /* no usable device / unsupported architecture */
+};
+
+/* Adam block geometry of a tensor. */
+enum {
+  BQ_ADAM_FLAT256 = 0, /* 256 consecutive elements (last block may be short) */
+  BQ_ADAM_TILE128 = 1  /* 128x128 tiles of the 2-D view (1-D tensors: 128 elements) */
+};
+
+/* One RaggedShard tensor: row-major 2-D view rows x cols (1-D: rows = 1), atomic
+ * block g in elements (a device boundary may only fall at a multiple of g from
+ * the tensor start), Adam block geometry, and whether it has 128x128 FP8 tiles. */
+typedef struct {
+  int64_t rows, cols, g;
+  int32_t adam_kind;
+  int32_t fp8;
+} bq_tensor_desc;
+
+/* Planner options.  alpha: collective alignment of S (elements); start_align:
+ * alignment of every tensor start (elements; the step kernels need a multiple of
+ * 8); order: 0 = the tensors' given order (the only order implemented). */
+typedef struct {
+  int64_t alpha;
+  int64_t start_align;
+  int32_t order;
+  int32_t reserved;
+} bq_plan_opts;
+
+typedef struct bq_layout bq_layout; /* planned DBuffer layout (host object) */
+typedef struct bq_shard bq_shard;   /* layout + device tables for [dev_lo, dev_hi) */
+
+typedef struct {
+  int64_t V, S, N;
+  int64_t n_intervals, n_mslots, n_fslots;
+  int64_t total_elems;   /* sum of tensor sizes */
+  int64_t padding_elems; /* V*S - total_elems */
+  int64_t export_len;    /* int64 entries written by bq_layout_export */
+  int64_t case3_prefix;  /* length of the winning Case-3 prefix */
+} bq_layout_info;
+
+/* fp32 Adam hyper-parameters; omb1 = 1-b1, omb2 = 1-b2, bc1 = 1-b1^t and
+ * bc2 = 1-b2^t are supplied by the caller (computed in fp64, rounded once). */
+typedef struct {
+  float lr, b1, b2, eps, omb1, omb2, bc1, bc2;
+} bq_adam_hp;
+
+/* One Newton-Schulz problem: bf16 row-major x (rows x cols, row pitch ld_x
+ * elements) -> bf16 y (same shape, pitch ld_y).  x and y may alias. */
+typedef struct {
+  const void* x;
+  void* y;
+  int64_t rows, cols, ld_x, ld_y;
+} bq_mat;
+
+const char* bq_strerror(int code);
+const char* bq_last_error(void);
+int bq_version(void);
+
+/* ------------------------------------------------------------------ planner
+ * bq_plan - lay out n tensors over V devices.
+ * Defined by: veScale-FSDP planning problem and heuristic (feynmanwiki
+ * walkthrough, paper section 5: equal local shards of size S, contiguous
+ * non-overlapping tensors with padding only between them, device boundaries only
+ * at multiples of g from a tensor's start, minimise S; default tensor order, DP
+ * feasibility per S, binary search over multiples of an LCM alignment, Case-3
+ * prefixes of the size-sorted tensors).
+ * t: host array of n descriptors (read only).  On success *out receives a new
+ * layout owned by the caller (free with bq_layout_free).  Errors: BQ_EINVAL for
+ * a bad descriptor (g not a multiple of the Adam block / FP8 band it must keep
+ * whole, or a 2-D FP8 / tile tensor with cols % 8 != 0), BQ_EINFEASIBLE never in
+ * practice (S = sum n + N*start_align always fits). */
+int bq_plan(const bq_tensor_desc* t, int n, int V, const bq_plan_opts* opts, bq_layout** out);
+void bq_layout_free(bq_layout* layout);
+int bq_layout_query(const bq_layout* layout, bq_layout_info* info);
+
+/* bq_layout_export - flat int64 table (host buffer buf of n entries):
+ *   header    [magic 0x4251, version 1, V, S, N, NI, n_mslots, n_fslots]
+ *   tensors   N  x [start, numel, rows, cols, g, adam_kind, fp8]
+ *   intervals NI x [dev, tensor, t_off, len, local_off, mslot, fslot]
+ *   devices   (V+1) x [first interval, mslot base, fslot base]
+ * Intervals are in device order, tensors in buffer order within a device; slots
+ * are numbered per device in interval order, inside an interval in tensor-flat
+ * order (256-element blocks) or band-major / column-tile-minor order (128x128
+ * tiles, 1-D: 128-element tiles).  fslot = -1 for tensors without FP8.
+ * BQ_ENOSPC if n < export_len. */
+int bq_layout_export(const bq_layout* layout, int64_t* buf, size_t n);
+
+/* ------------------------------------------------------------------ device tables
+ * bq_layout_upload - derive the work tables of local shards [dev_lo, dev_hi) and
+ * copy them into the caller's device workspace dev_ws (ws_bytes, query with
+ * bq_layout_upload_bytes) on stream.  *out receives a host bq_shard (free with
+ * bq_shard_free) that the step calls take; the workspace must stay alive and
+ * unmodified while the shard is used.  BQ_EALIGN if an interval's local offset
+ * is not a multiple of 8 elements (plan with start_align % 8 == 0). */
+int bq_layout_upload_bytes(const bq_layout* layout, int dev_lo, int dev_hi, size_t* bytes);
+int bq_layout_upload(const bq_layout* layout, int dev_lo, int dev_hi, void* dev_ws, size_t ws_bytes,
+                     bq_stream_t stream, bq_shard** out);
+void bq_shard_free(bq_shard* shard);
+
+/* ------------------------------------------------------------------ step
+ * bq_pack - group-level fused pre-communication add / scale / zero / copy.
+ * Defined by: DBuffer's fused pre-communication ops (bud-325 summary, Key claims
+ * and Method; feynmanwiki walkthrough, paper section 5, DBuffer paragraphs).
+ * For every element j of every interval (dev, i, t_off, len, local_off) in range:
+ *   y = f32(grad_i[t_off + j]) * scale; if accumulate: y = f32(dbuf[pos]) + y;
+ *   dbuf[pos] = bf16_rne(y)  (pos = (dev-dev_lo)*S + local_off + j)
+ * and every padding element of the range is set to +0.
+ * grad_ptrs: DEVICE array of N device pointers, grad_ptrs[i] = address of element
+ * 0 of tensor i (bf16); only the owned elements are read, so a pointer may be a
+ * virtual base below an allocation that holds just the owned range.
+ * dbuf_grad: bf16, (dev_hi-dev_lo)*S elements. */
+int bq_pack(const bq_shard* shard, const void* const* grad_ptrs, void* dbuf_grad, float scale, int accumulate,
+            bq_stream_t stream);
+
+/* bq_step_adam8 - block-wise 8-bit Adam on the local shards, optionally fused with
+ * the FP8 requantisation of the updated parameters.
+ * Defined by: 8-bit Adam with per-block quantised state kept device-local by
+ * RaggedShard granularity (bud-325 summary, Key claims; feynmanwiki walkthrough,
+ * paper section 6.3) and block-wise FP8 (DeepSeek-V3 style, bud-325 TL;DR).
+ * Per element, each an IEEE fp32 op rounded to nearest, no FMA:
+ *   g=f32(grad); m=qm*sm; v=qv*sv; m'=b1*m+omb1*g; v'=b2*v+omb2*(g*g);
+ *   p'=p-lr*((m'/bc1)/(sqrt(v'/bc2)+eps))
+ * per Adam block: sm'=max|m'|/127, qm'=clamp(rint(m'/sm'),-127,127);
+ *   sv'=max v'/255, qv'=clamp(rint(v'/sv'),0,255); all-zero block -> scale 0.
+ * per FP8 tile (if fp8_out != NULL): s=max|p'|/448, code=e4m3_rne_satfinite(p'/s);
+ *   all-zero tile -> s=0, codes +-0.
+ * grad: bf16 packed buffer; master fp32, m int8, v uint8, fp8_out uint8 - all
+ * (dev_hi-dev_lo)*S elements, updated in place (padding untouched); m_scale,
+ * v_scale: fp32 per Adam slot; fp8_scale: fp32 per FP8 slot.  hp: host pointer. */
+int bq_step_adam8(const bq_shard* shard, const void* grad, float* master, int8_t* m, uint8_t* v, float* m_scale,
+                  float* v_scale, const bq_adam_hp* hp, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream);
+
+/* bq_quant_fp8 - standalone FP8 requantisation of master into fp8_out / fp8_scale
+ * (same tile rule as above). */
+int bq_quant_fp8(const bq_shard* shard, const float* master, uint8_t* fp8_out, float* fp8_scale,
+                 bq_stream_t stream);
+
+/* ------------------------------------------------------------------ Muon
+ * bq_muon_ns - Newton-Schulz orthogonalisation of `batch` whole matrices.
+ * Defined by: Muon's matrix-sign preconditioner run at one root on the complete
+ * 2-D matrix (feynmanwiki walkthrough, paper section 6.3).  Per matrix (a tall
+ * one is iterated as its transpose and written back transposed):
+ *   X = x / (||x||_F + eps); repeat steps: A = X X^T; B = b A + c A A; X = a X + B X
+ * on tcgen05 tensor cores: bf16 operands, fp32 accumulation, bf16 storage of
+ * X, A, B between products, fp32 Frobenius norm.
+ * mats: host array; ws: device workspace of ws_bytes (bf16 scratch for X, A, B
+ * and a few fp32 words), size from bq_muon_ns_workspace. */
+int bq_muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes);
+int bq_muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws,
+               size_t ws_bytes, bq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BQ_H */

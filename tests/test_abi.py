@@ -1,0 +1,169 @@
+"""The C ABI on the host (no GPU): the library loads and exports every entry point
+include/bq.h declares, the C++ planner's exported table equals the oracle's bit
+for bit, and host-detectable errors come back as codes."""
+
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import block_quant_gb300 as bq
+import workloads as W
+from oracle import planner as P
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "bq.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_quant_gb300 import build
+
+    build.build()
+    return bq.load()
+
+
+def test_exports_every_declared_symbol(built):
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)  # drop comments
+    declared = sorted(set(re.findall(r"\b(bq_[a-z0-9_]+)\s*\(", src)))
+    assert declared, "no declarations found"
+    assert sorted(bq.SYMBOLS) == declared
+    for name in declared:
+        assert hasattr(built, name), name
+    assert built.bq_version() == 1
+    assert built.bq_strerror(bq.BQ_EALIGN) == b"misaligned pointer or offset"
+
+
+def _oracle_export(descs, V, alpha, start_align):
+    return np.asarray(P.plan(descs, V, alpha, start_align).export(), np.int64)
+
+
+def _descs(unit):
+    return [P.TensorDesc(t.rows, t.cols, t.g, t.adam_kind, t.fp8) for t in unit.tensors]
+
+
+@pytest.mark.parametrize("name", W.NAMED[:4] + W.SMALL[1:4])
+def test_planner_matches_oracle_on_configs(name):
+    c = W.config(name)
+    for u in c.units:
+        want = _oracle_export(_descs(u), c.V, c.alpha, c.start_align)
+        got = bq.plan(u.tensors, c.V, c.alpha, c.start_align).export()
+        assert np.array_equal(got, want), (name, u.name)
+
+
+def test_planner_matches_oracle_on_random_groups():
+    rng = np.random.default_rng(17)
+    for trial in range(300):
+        N = int(rng.integers(1, 9))
+        descs = []
+        for _ in range(N):
+            if rng.random() < 0.4:  # 1-D
+                rows, cols = 1, int(rng.integers(1, 3000))
+                kind = int(rng.integers(0, 2))
+                unit = 256 if kind == 0 else 128
+                g = unit * int(rng.choice([1, 2, 3]))
+                fp8 = bool(rng.random() < 0.5)
+            else:
+                rows = int(rng.integers(1, 700))
+                cols = 8 * int(rng.integers(1, 90))
+                kind = int(rng.integers(0, 2))
+                band = 128 * cols
+                g = band * int(rng.choice([1, 2]))
+                if kind == 0:
+                    g = int(np.lcm(g, 256))
+                fp8 = bool(rng.random() < 0.7)
+            descs.append(P.TensorDesc(rows, cols, g, kind, fp8))
+        V = int(rng.integers(1, 17))
+        alpha = int(rng.choice([1, 8, 128, 1000]))
+        align = int(rng.choice([1, 8, 16]))
+        want = _oracle_export(descs, V, alpha, align)
+        got = bq.plan(descs, V, alpha, align).export()
+        assert np.array_equal(got, want), (trial, [(d.rows, d.cols, d.g, d.adam_kind, d.fp8) for d in descs], V)
+
+
+def test_planner_tiny_granularities_match_oracle():
+    rng = np.random.default_rng(23)
+    for _ in range(500):
+        N = int(rng.integers(1, 7))
+        gs = [int(rng.choice([256, 512, 768])) for _ in range(N)]
+        ns = [int(rng.integers(1, 9)) * 256 + int(rng.integers(0, 300)) for _ in range(N)]
+        descs = [P.TensorDesc(1, n, g, 0, False) for n, g in zip(ns, gs)]
+        V = int(rng.integers(1, 8))
+        got = bq.plan(descs, V, 1, 1).export()
+        assert np.array_equal(got, _oracle_export(descs, V, 1, 1))
+
+
+def test_planner_rejects_bad_descriptors():
+    with pytest.raises(bq.BQError) as e:
+        bq.plan([(1, 1000, 100, bq.ADAM_FLAT256, 0)], 4)  # g not a multiple of 256
+    assert e.value.code == bq.BQ_EINVAL
+    with pytest.raises(bq.BQError) as e:
+        bq.plan([(256, 100, 128 * 100, bq.ADAM_TILE128, 1)], 4)  # cols % 8 != 0 for 2-D tiles
+    assert e.value.code == bq.BQ_EINVAL
+    with pytest.raises(bq.BQError) as e:
+        bq.plan([(256, 64, 64, bq.ADAM_TILE128, 0)], 4)  # g splits a 128-row band
+    assert e.value.code == bq.BQ_EINVAL
+    with pytest.raises(bq.BQError) as e:
+        bq.plan([], 4)
+    assert e.value.code == bq.BQ_EINVAL
+    with pytest.raises(bq.BQError) as e:
+        bq.plan([(1, 256, 256, 7, 0)], 4)
+    assert e.value.code == bq.BQ_EINVAL
+
+
+def test_export_needs_room_and_upload_checks_alignment(built):
+    L = bq.plan([(1, 1000, 256, 0, 0), (1, 999, 256, 0, 0)], 3, alpha=1, start_align=1)
+    buf = np.zeros(5, np.int64)
+    rc = built.bq_layout_export(L.handle, buf.ctypes.data_as(C.POINTER(C.c_int64)), 5)
+    assert rc == bq.BQ_ENOSPC
+    info = L.info()
+    # start_align 1 leaves a local offset that is not a multiple of 8: the step
+    # kernels refuse such a layout before touching the device
+    iv = W.Table(L.export()).intervals
+    if np.any(iv[:, 4] % 8):
+        with pytest.raises(bq.BQError) as e:
+            L.upload_bytes(0, info["V"])
+        assert e.value.code == bq.BQ_EALIGN
+    with pytest.raises(bq.BQError) as e:
+        L.upload_bytes(2, 1)
+    assert e.value.code == bq.BQ_EINVAL
+    L2 = bq.plan([(1, 1000, 256, 0, 0)], 2)
+    assert L2.upload_bytes(0, 2) > 0
+    with pytest.raises(bq.BQError) as e:
+        L2.upload(0, 2, 0, 1 << 20, stream=0)  # NULL workspace
+    assert e.value.code == bq.BQ_EALIGN
+
+
+def test_layout_info_consistent():
+    c = W.config("gptoss-small")
+    L = bq.plan(c.units[0].tensors, c.V, c.alpha, c.start_align)
+    inf = L.info()
+    t = W.Table(L.export())
+    assert inf["S"] == t.S and inf["n_intervals"] == t.NI and inf["n_mslots"] == t.n_mslots
+    assert inf["total_elems"] == sum(x.numel for x in c.units[0].tensors)
+    assert inf["padding_elems"] == c.V * inf["S"] - inf["total_elems"]
+
+
+def test_shard_tables_pass_host_bounds_check():
+    """bq_layout_upload_bytes builds the kernels' work tables and checks every
+    element range and scale slot against the shard range on the host; run it on
+    every layout the GPU tests use, at every device range they use."""
+    import sys
+
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from test_parity_step import _edge_tensors
+
+    cases = []
+    for name in W.NAMED[:4] + W.SMALL[:4]:
+        c = W.config(name)
+        for u in c.units:
+            cases.append((u.tensors, c.V, c.alpha, c.start_align))
+    for V in (1, 2, 3, 5, 6):
+        cases.append((_edge_tensors(), V, 128, 16))
+    for tensors, V, alpha, align in cases:
+        L = bq.plan(tensors, V, alpha, align)
+        ranges = {(0, V), (0, 1), (V - 1, V), (V // 2, V)}
+        for lo, hi in ranges:
+            if lo < hi:
+                assert L.upload_bytes(lo, hi) > 0

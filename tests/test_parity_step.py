@@ -1,0 +1,108 @@
+"""CUDA path vs oracle for the DBuffer step (pack + 8-bit Adam + FP8), element by
+element, through the C ABI.  Codes, scales, packed gradients and the fp32 master
+must agree bit for bit (the contract allows 1e-6 relative on the master; the
+kernels use the same fp32 operation order, so exact agreement is required and any
+mismatch is reported)."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from _step_harness import StepCase, assert_bits_equal
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(case, got, want, fp8=True):
+    assert_bits_equal("dbuf", got["dbuf"], want["dbuf"])
+    assert_bits_equal("master", got["master"], want["master"])
+    assert_bits_equal("m codes", got["m"], want["m"])
+    assert_bits_equal("v codes", got["v"], want["v"])
+    assert_bits_equal("m scales", got["ms"], want["ms"])
+    assert_bits_equal("v scales", got["vs"], want["vs"])
+    if fp8:
+        assert_bits_equal("fp8 codes (fused)", got["fp8"], want["fp8"])
+        assert_bits_equal("fp8 scales (fused)", got["fs"], want["fs"])
+    assert_bits_equal("fp8 codes (standalone)", got["q2"], want["fp8"])
+    assert_bits_equal("fp8 scales (standalone)", got["s2"], want["fs"])
+
+
+@pytest.mark.parametrize("name,dev", [
+    ("toy", None), ("toy", (1, 3)),
+    ("llama-small", None), ("llama-small", (3, 6)),
+    ("llama-tile-small", None), ("llama-tile-small", (1, 2)),
+    ("gptoss-small", None), ("gptoss-small", (2, 7)),
+])
+def test_step_matches_oracle(cuda, name, dev):
+    c = W.config(name)
+    kw = {} if dev is None else dict(dev_lo=dev[0], dev_hi=dev[1])
+    case = StepCase(c, **kw)
+    _compare(case, case.run_gpu(cuda), case.run_oracle())
+
+
+def test_step_without_fp8_output(cuda):
+    case = StepCase(W.config("llama-small"))
+    got = case.run_gpu(cuda, fp8=False)
+    _compare(case, got, case.run_oracle(), fp8=False)
+
+
+def test_pack_accumulate_and_scale(cuda):
+    case = StepCase(W.config("gptoss-small"), dev_lo=0, dev_hi=3)
+    got = case.run_gpu(cuda, scale=0.37, accumulate=True)
+    _compare(case, got, case.run_oracle(scale=0.37, accumulate=True))
+
+
+def test_first_step_from_zero_state(cuda):
+    case = StepCase(W.config("llama-tile-small"), t=1, zero_state=True)
+    _compare(case, case.run_gpu(cuda), case.run_oracle())
+    case = StepCase(W.config("gptoss-small"), t=1, zero_state=True)
+    _compare(case, case.run_gpu(cuda), case.run_oracle())
+
+
+def _edge_tensors():
+    T = W.TensorSpec
+    return [
+        T("ragged_1d", 1, 1001, 256, W.ADAM_FLAT256, True),      # tail not a multiple of 8
+        T("tiny_1d", 1, 3, 256, W.ADAM_FLAT256, True),           # shorter than one vector
+        T("tile_1d", 1, 300, 128, W.ADAM_TILE128, True),         # 128-element tiles, ragged
+        T("band_2d", 200, 360, 128 * 360, W.ADAM_FLAT256, True), # blocks straddle rows, ragged band
+        T("strip_2d", 130, 512, 128 * 512, W.ADAM_FLAT256, True),
+        T("tile_2d", 140, 200, 128 * 200, W.ADAM_TILE128, True), # clipped tiles both ways
+        T("tile_2d_nofp8", 129, 136, 128 * 136, W.ADAM_TILE128, False),
+        T("zero_2d", 128, 256, 128 * 256, W.ADAM_FLAT256, True), # all-zero grads, params: zero scales
+        T("plain_2d", 100, 24, 256 * 3, W.ADAM_FLAT256, False),
+    ]
+
+
+@pytest.mark.parametrize("V,dev", [(1, (0, 1)), (3, (0, 3)), (5, (1, 4))])
+def test_edge_shapes(cuda, V, dev):
+    c = W.config("toy")
+    c.cfg_id = 40
+    case = StepCase(c, tensors=_edge_tensors(), V=V, dev_lo=dev[0], dev_hi=dev[1], zero_tensors=(7,))
+    _compare(case, case.run_gpu(cuda), case.run_oracle())
+
+
+def test_zero_state_and_zero_tensor(cuda):
+    c = W.config("toy")
+    c.cfg_id = 41
+    case = StepCase(c, tensors=_edge_tensors(), V=2, dev_lo=0, dev_hi=2, zero_state=True, t=1,
+                    zero_tensors=(0, 5, 7))
+    got = case.run_gpu(cuda)
+    want = case.run_oracle()
+    _compare(case, got, want)
+    assert np.any(want["ms"] == 0)  # the all-zero blocks really took the zero-scale path
+
+
+def test_padding_only_devices(cuda):
+    """A tensor much smaller than the buffer: some devices hold only padding."""
+    c = W.config("toy")
+    c.cfg_id = 42
+    T = W.TensorSpec
+    tensors = [T("a", 1, 512, 256, W.ADAM_FLAT256, True), T("b", 1, 256, 256, W.ADAM_FLAT256, True)]
+    case = StepCase(c, tensors=tensors, V=6, dev_lo=0, dev_hi=6)
+    _compare(case, case.run_gpu(cuda), case.run_oracle())
+    empty = StepCase(c, tensors=tensors, V=6, dev_lo=4, dev_hi=6)
+    got = empty.run_gpu(cuda)
+    assert not got["dbuf"].any()
+    _compare(empty, got, empty.run_oracle())
