@@ -149,7 +149,7 @@ class Clocks:
 class DBufferStep:
     """Device-resident buffers of one unit's DBuffer step (all V local shards)."""
 
-    def __init__(self, cfg, dev, seed):
+    def __init__(self, cfg, dev, seed, shards=None):
         import torch
 
         import block_quant_gb300 as bq
@@ -157,6 +157,8 @@ class DBufferStep:
         self.bq, self.torch, self.dev = bq, torch, dev
         unit = cfg.units[0]
         self.V, self.lo, self.hi = cfg.V, cfg.dev_lo, cfg.dev_hi
+        if shards:
+            self.hi = self.lo + shards
         self.layout = bq.plan(unit.tensors, cfg.V, cfg.alpha, cfg.start_align)
         self.table = W.Table(self.layout.export())
         S = self.table.S
@@ -280,7 +282,7 @@ def run_ours(args):
 
     bq.load()
     cfg = W.config(WORKLOAD)
-    step = DBufferStep(cfg, dev, seed=1000 + rank)
+    step = DBufferStep(cfg, dev, seed=1000 + rank, shards=args.shards)
     muon = MuonBatch(W.config(MUON).muon_shapes, dev, seed=2000 + rank) if args.muon else None
     stream = torch.cuda.current_stream(dev)
 
@@ -364,9 +366,8 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {
-                "workload": "llama3-8b-layer DBuffer step (V=8, all 8 local shards) + Muon NS batch "
-                            "[4096x4096, 4096x14336, 14336x4096] x 5 iterations" if muon else
-                            "llama3-8b-layer DBuffer step (V=8, all 8 local shards)",
+                "workload": f"llama3-8b-layer DBuffer step (V=8, local shards {step.lo}..{step.hi - 1})" +
+                            (" + Muon NS batch [4096x4096, 4096x14336, 14336x4096] x 5 iterations" if muon else ""),
                 "elements": step.bytes["elems"], "padding_elements": step.bytes["pads"], "S": step.table.S,
                 "bytes_per_step": B, "l2": f"inputs {step.n * 13 / 1e9:.1f} GB > L2: no flush needed",
                 "parallelism": f"dp{world}: one independent layer per GPU, no data-path collective",
@@ -438,6 +439,8 @@ def main():
     ap.add_argument("--muon", dest="muon", action="store_true", default=True)
     ap.add_argument("--no-muon", dest="muon", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shards", type=int, default=None,
+                    help="process only local shards [0, K) of the DBuffer (smaller case for profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -39,7 +39,8 @@ using namespace bq;
 struct bq_shard {
   const bq_layout* layout;
   int dev_lo, dev_hi;
-  int64_t total;  // elements of the shard range
+  int64_t total;           // elements of the shard range
+  int64_t nm, nf;          // Adam / FP8 scale slots of the range
   DevTables dev;
 };
 
@@ -150,6 +151,8 @@ int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, s
   sh->dev_lo = dev_lo;
   sh->dev_hi = dev_hi;
   sh->total = int64_t(dev_hi - dev_lo) * L->S;
+  sh->nm = L->dev_mslot[dev_hi] - L->dev_mslot[dev_lo];
+  sh->nf = L->dev_fslot[dev_hi] - L->dev_fslot[dev_lo];
   auto* base = static_cast<unsigned char*>(dev_ws);
   sh->dev.pieces = reinterpret_cast<const PackPiece*>(base + p.off_pieces);
   sh->dev.chunk_first = reinterpret_cast<const int32_t*>(base + p.off_chunks);
@@ -181,10 +184,12 @@ int bq_pack(const bq_shard* sh, const void* const* grad_ptrs, void* dbuf_grad, f
 
 int bq_step_adam8(const bq_shard* sh, const void* grad, float* master, int8_t* m, uint8_t* v, float* m_scale,
                   float* v_scale, const bq_adam_hp* hp, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream) {
-  if (!sh || !grad || !master || !m || !v || !m_scale || !v_scale || !hp)
-    return set_error(BQ_EINVAL, "bq_step_adam8: NULL argument");
-  if ((fp8_out == nullptr) != (fp8_scale == nullptr))
-    return set_error(BQ_EINVAL, "bq_step_adam8: fp8_out and fp8_scale must both be set or both NULL");
+  if (!sh || !grad || !master || !m || !v || !hp) return set_error(BQ_EINVAL, "bq_step_adam8: NULL argument");
+  // scale buffers may be NULL only when the range has no slots of that kind
+  if (sh->nm > 0 && (!m_scale || !v_scale)) return set_error(BQ_EINVAL, "bq_step_adam8: NULL scale buffer");
+  if (fp8_out && !fp8_scale && sh->nf > 0)
+    return set_error(BQ_EINVAL, "bq_step_adam8: fp8_out needs fp8_scale");
+  if (!fp8_out && fp8_scale) return set_error(BQ_EINVAL, "bq_step_adam8: fp8_scale without fp8_out");
   const void* ptrs[] = {grad, master, m, v, fp8_out};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return set_error(BQ_EALIGN, "bq_step_adam8: buffers must be 16-byte aligned");
@@ -196,7 +201,8 @@ int bq_step_adam8(const bq_shard* sh, const void* grad, float* master, int8_t* m
 }
 
 int bq_quant_fp8(const bq_shard* sh, const float* master, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream) {
-  if (!sh || !master || !fp8_out || !fp8_scale) return set_error(BQ_EINVAL, "bq_quant_fp8: NULL argument");
+  if (!sh || !master || !fp8_out) return set_error(BQ_EINVAL, "bq_quant_fp8: NULL argument");
+  if (!fp8_scale && sh->nf > 0) return set_error(BQ_EINVAL, "bq_quant_fp8: NULL fp8_scale");
   if (!aligned16(master) || !aligned16(fp8_out) || (reinterpret_cast<uintptr_t>(fp8_scale) & 3))
     return set_error(BQ_EALIGN, "bq_quant_fp8: misaligned buffer");
   return launch_quant_fp8(sh->dev, master, fp8_out, fp8_scale, stream);
