@@ -49,7 +49,7 @@ class LayoutInfo(C.Structure):
 
 
 class AdamHp(C.Structure):
-    _fields_ = [(n, C.c_float) for n in ("lr", "b1", "b2", "eps", "omb1", "omb2", "bc1", "bc2")]
+    _fields_ = [(n, C.c_float) for n in ("lr", "b1", "b2", "eps", "omb1", "omb2", "rbc1", "rbc2")]
 
 
 class Mat(C.Structure):
@@ -202,9 +202,10 @@ def plan(descs, V, alpha=128, start_align=16):
 
 
 def adam_hparams(lr, b1, b2, eps, t):
-    """fp32 hyper-parameters; the derived ones in fp64, rounded once."""
+    """fp32 hyper-parameters; the derived ones (1-b1, 1-b2 and the reciprocal bias
+    corrections 1/(1-b^t)) in fp64, rounded once."""
     lr, b1, b2, eps = float(lr), float(b1), float(b2), float(eps)
-    return AdamHp(lr, b1, b2, eps, 1.0 - b1, 1.0 - b2, 1.0 - b1 ** t, 1.0 - b2 ** t)
+    return AdamHp(lr, b1, b2, eps, 1.0 - b1, 1.0 - b2, 1.0 / (1.0 - b1 ** t), 1.0 / (1.0 - b2 ** t))
 
 
 def pack(shard, grad_ptrs, dbuf_grad, scale, accumulate=False, stream=None):

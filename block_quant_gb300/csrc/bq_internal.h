@@ -72,7 +72,24 @@ struct RegionGroup {
   int64_t pos;
   int32_t rows, C, c0, width;
   int32_t mslot, fslot;
+  uint32_t cmul, cshr;  // n / C == umulhi(n, cmul) >> cshr for 0 <= n < 2^31 (cmul 0: C == 1)
 };
+
+// Division by an invariant integer with a multiply and a shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// with l = ceil(log2 d) and m = ceil(2^(31+l) / d), floor(n / d) equals
+// floor(n * m / 2^(31+l)) for every 0 <= n < 2^31.
+inline void make_fastdiv(uint32_t d, uint32_t* mul, uint32_t* shr) {
+  if (d <= 1) {
+    *mul = 0;
+    *shr = 0;
+    return;
+  }
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  *mul = uint32_t(((uint64_t(1) << (31 + l)) + d - 1) / d);
+  *shr = l - 1;
+}
 
 struct ShardTables {
   std::vector<PackPiece> pieces;

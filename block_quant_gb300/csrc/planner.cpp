@@ -317,6 +317,8 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
       const int64_t C = t.cols;
       const int64_t r0 = v.t_off / C, r1 = (v.t_off + v.len) / C;
       const int64_t nct = ceil_div(C, 128);
+      uint32_t cmul, cshr;
+      make_fastdiv(uint32_t(C), &cmul, &cshr);
       for (int64_t rb = r0, band = 0; rb < r1; rb += 128, ++band) {
         const int32_t rows = int32_t(std::min<int64_t>(128, r1 - rb));
         const int64_t bpos = pos0 + (rb - r0) * C;
@@ -326,18 +328,20 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
             const int64_t c0 = ct * 128;
             T.tiles.push_back(RegionGroup{bpos + c0, rows, int32_t(C), int32_t(c0),
                                           int32_t(std::min<int64_t>(128, C - c0)),
-                                          int32_t(mslot + band * nct + ct), fband < 0 ? -1 : int32_t(fband + ct)});
+                                          int32_t(mslot + band * nct + ct), fband < 0 ? -1 : int32_t(fband + ct),
+                                          cmul, cshr});
           }
         } else {
           // FLAT256 Adam + FP8: flat block index of the band start
           const int32_t mband = int32_t(mslot + (rb - r0) * C / 256);
           if (C % 256 == 0) {
+            // 256-column strips: every Adam block is one row segment of the strip
             for (int64_t c0 = 0; c0 < C; c0 += 256)
               T.strips.push_back(RegionGroup{bpos + c0, rows, int32_t(C), int32_t(c0), 256,
-                                             int32_t(mband + c0 / 256), int32_t(fband + c0 / 128)});
+                                             int32_t(mband + c0 / 256), int32_t(fband + c0 / 128), cmul, cshr});
             T.max_strip_tiles = std::max(T.max_strip_tiles, 2);
           } else {
-            T.strips.push_back(RegionGroup{bpos, rows, int32_t(C), 0, int32_t(C), mband, fband});
+            T.strips.push_back(RegionGroup{bpos, rows, int32_t(C), 0, int32_t(C), mband, fband, cmul, cshr});
             T.max_strip_tiles = std::max<int32_t>(T.max_strip_tiles, int32_t(nct));
           }
         }
@@ -379,7 +383,8 @@ std::string validate_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, co
     if (g.rows <= 0 || g.rows > 128 || g.C % 8 || g.width % 8 || g.pos % 8 || g.pos < 0) return "strip shape";
     const int64_t last = flat ? g.pos + int64_t(g.rows) * g.C : g.pos + int64_t(g.rows - 1) * g.C + g.width;
     if (last > total) return "strip reads outside the shard range";
-    if (!flat && (g.C % 256 || g.c0 % 256 || g.width % 256 || g.c0 + g.width > g.C)) return "strip columns";
+    if (!flat && (g.C % 256 || g.c0 % 256 || g.width != 256 || g.c0 + g.width > g.C)) return "strip columns";
+    if (int64_t(g.rows) * g.C >= (int64_t(1) << 31)) return "strip band too large for 32-bit offsets";
     const int64_t mend = flat ? g.mslot + ceil_div(int64_t(g.rows) * g.C, 256)
                               : g.mslot + int64_t(g.rows - 1) * (g.C / 256) + g.width / 256;
     if (g.mslot < 0 || mend > nm) return "strip Adam slots out of range";

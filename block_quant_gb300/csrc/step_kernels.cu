@@ -26,6 +26,12 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+// resident CTAs per SM the Adam kernels are compiled for (register budget) and
+// launched with (grid-stride kernels)
+#ifndef BQ_ADAM_CTAS_PER_SM
+#define BQ_ADAM_CTAS_PER_SM 3
+#endif
+constexpr int kAdamCtas = BQ_ADAM_CTAS_PER_SM;
 
 // ---------------------------------------------------------------- element helpers
 
@@ -36,89 +42,143 @@ __device__ __forceinline__ uint32_t f2bf(float x) {
 }
 
 struct Hp {
-  float lr, b1, b2, eps, omb1, omb2, bc1, bc2;
+  float lr, b1, b2, eps, omb1, omb2, rbc1, rbc2;
 };
 
-__device__ __forceinline__ void adam_elem(const Hp& h, float g, float p, float qm, float qv, float sm, float sv,
-                                          float& p1, float& m1, float& v1) {
-  const float m = __fmul_rn(qm, sm);
-  const float v = __fmul_rn(qv, sv);
-  m1 = __fadd_rn(__fmul_rn(h.b1, m), __fmul_rn(h.omb1, g));
-  v1 = __fadd_rn(__fmul_rn(h.b2, v), __fmul_rn(h.omb2, __fmul_rn(g, g)));
-  const float mh = __fdiv_rn(m1, h.bc1);
-  const float vh = __fdiv_rn(v1, h.bc2);
-  const float den = __fadd_rn(__fsqrt_rn(vh), h.eps);
-  p1 = __fsub_rn(p, __fmul_rn(h.lr, __fdiv_rn(mh, den)));
+__device__ __forceinline__ Hp make_hp(const bq_adam_hp& h) {
+  return Hp{h.lr, h.b1, h.b2, h.eps, h.omb1, h.omb2, h.rbc1, h.rbc2};
 }
 
-// scale from an absmax (as fp32 bits; all values >= 0 so bit order == value order)
-__device__ __forceinline__ float scale_of(uint32_t amax_bits, float qmax) {
-  return amax_bits ? __fdiv_rn(__uint_as_float(amax_bits), qmax) : 0.f;
+// Blackwell's packed fp32 pair multiply: each component is rounded exactly like
+// the scalar round-to-nearest multiply.  Additions stay scalar (__fadd_rn):
+// ptxas contracts a packed multiply feeding a packed add into a fused
+// multiply-add even when both carry an explicit .rn, which would change results;
+// a scalar .rn add is never contracted.
+__device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2s(float2 a, float2 b) {
+  return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
 }
 
-__device__ __forceinline__ uint32_t q_int8(float x, float s) {
-  if (s == 0.f) return 0u;
-  const float r = fminf(fmaxf(rintf(__fdiv_rn(x, s)), -127.f), 127.f);
-  return uint32_t(int32_t(r)) & 0xFFu;
+// The Adam update of two elements; per element, every step one IEEE fp32 op
+// rounded to nearest, no FMA:
+//   m' = b1*m + omb1*g;  v' = b2*v + omb2*(g*g);  mh = m'*rbc1;  vh = v'*rbc2;
+//   p' = p - lr*(mh/(sqrt(vh)+eps))
+__device__ __forceinline__ void adam_pair(const Hp& h, float2 g, float2 p, float2 qm, float2 qv, float2 sm, float2 sv,
+                                          float2& p1, float2& m1, float2& v1) {
+  const float2 m = mul2(qm, sm), v = mul2(qv, sv);
+  m1 = add2s(mul2(dup(h.b1), m), mul2(dup(h.omb1), g));
+  v1 = add2s(mul2(dup(h.b2), v), mul2(dup(h.omb2), mul2(g, g)));
+  const float2 mh = mul2(m1, dup(h.rbc1)), vh = mul2(v1, dup(h.rbc2));
+  const float2 den = add2s(make_float2(__fsqrt_rn(vh.x), __fsqrt_rn(vh.y)), dup(h.eps));
+  const float2 u = make_float2(__fdiv_rn(mh.x, den.x), __fdiv_rn(mh.y, den.y));
+  const float2 lu = mul2(dup(h.lr), u);
+  p1 = make_float2(__fsub_rn(p.x, lu.x), __fsub_rn(p.y, lu.y));
 }
 
-__device__ __forceinline__ uint32_t q_uint8(float x, float s) {
-  if (s == 0.f) return 0u;
-  const float r = fminf(fmaxf(rintf(__fdiv_rn(x, s)), 0.f), 255.f);
-  return uint32_t(r);
-}
-
-__device__ __forceinline__ uint32_t q_e4m3(float x, float s) {
-  if (s == 0.f) return (__float_as_uint(x) >> 24) & 0x80u;  // +-0 keeps its sign
-  return uint32_t(__nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3));
-}
-
-// 8 consecutive elements at a 16-byte-aligned (bf16) / 32-byte-aligned (fp32) spot
-struct Vec8 {
-  float g[8], p[8], qm[8], qv[8];
+// Block scale from an absmax (fp32 bits; all values >= 0 so bit order == value
+// order): stored scale s = amax/qmax, reciprocal r = qmax/amax (one division each
+// per block).  mode 0: s == 0 -> zero codes; 1: codes from x*r; 2: r overflowed
+// (tiny amax) -> codes from x/s.
+struct QScale {
+  float s, r;
+  int mode;
 };
 
-__device__ __forceinline__ void load8(const AdamArgs& a, int64_t pos, Vec8& x) {
-  const uint4 gr = *reinterpret_cast<const uint4*>(a.grad + pos);
-  const float4 p0 = *reinterpret_cast<const float4*>(a.master + pos);
-  const float4 p1 = *reinterpret_cast<const float4*>(a.master + pos + 4);
-  const uint2 mm = *reinterpret_cast<const uint2*>(a.m + pos);
-  const uint2 vv = *reinterpret_cast<const uint2*>(a.v + pos);
-  const uint32_t gw[4] = {gr.x, gr.y, gr.z, gr.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x.g[2 * i] = bf16f(gw[i] & 0xFFFFu);
-    x.g[2 * i + 1] = bf16f(gw[i] >> 16);
-  }
-  x.p[0] = p0.x; x.p[1] = p0.y; x.p[2] = p0.z; x.p[3] = p0.w;
-  x.p[4] = p1.x; x.p[5] = p1.y; x.p[6] = p1.z; x.p[7] = p1.w;
-  const uint32_t mw[2] = {mm.x, mm.y}, vw[2] = {vv.x, vv.y};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x.qm[i] = float(int8_t((mw[i >> 2] >> (8 * (i & 3))) & 0xFFu));
-    x.qv[i] = float((vw[i >> 2] >> (8 * (i & 3))) & 0xFFu);
-  }
+__device__ __forceinline__ QScale qscale(uint32_t amax_bits, float qmax) {
+  const float a = __uint_as_float(amax_bits);
+  QScale q;
+  q.s = __fdiv_rn(a, qmax);
+  q.r = __fdiv_rn(qmax, a);
+  q.mode = q.s == 0.f ? 0 : (isinf(q.r) ? 2 : 1);
+  return q;
 }
 
-// masked scalar version for a short tail (n valid elements, n < 8)
-__device__ __forceinline__ void load_tail(const AdamArgs& a, int64_t pos, int n, Vec8& x) {
+// Exact small-integer conversions without I2F / F2I:
+//  * a byte b placed in the low mantissa bits of 2^23 (bit pattern 0x4B0000bb)
+//    is the float 2^23 + b, so subtracting 2^23 gives float(b) exactly (a signed
+//    byte is first offset by 128 by flipping its top bit);
+//  * for |y| < 2^22, y + 1.5*2^23 rounds y to the nearest integer, ties to even
+//    (the add's own rounding), and the low byte of the sum's bit pattern is that
+//    integer modulo 256 (two's complement for negative values).
+__device__ __forceinline__ float2 byte_pair(uint32_t w, int i, float bias) {
+  const float2 t = make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | uint32_t(i))),
+                               __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | uint32_t(i + 1))));
+  return add2s(t, dup(-bias));
+}
+
+// low bytes of four words -> one word
+__device__ __forceinline__ uint32_t low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
+// 8 int8 codes, packed little-endian into two words.  On the reciprocal path
+// |x * r| <= 127 (1 + 2^-23) because |x| <= amax, so the rounded value already
+// lies in [-127, 127] and needs no clamp; the division path (tiny blocks, whose
+// subnormal scale may be inexact) clamps.
+__device__ __forceinline__ uint2 codes_int8(const float* x, const QScale& q) {
+  if (q.mode == 0) return make_uint2(0u, 0u);
+  uint32_t b[8];
+  if (q.mode == 1) {
+    const float2 r = dup(q.r), k = dup(12582912.f);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const bool ok = i < n;
-    x.g[i] = ok ? bf16f(a.grad[pos + i]) : 0.f;
-    x.p[i] = ok ? a.master[pos + i] : 0.f;
-    x.qm[i] = ok ? float(a.m[pos + i]) : 0.f;
-    x.qv[i] = ok ? float(a.v[pos + i]) : 0.f;
+    for (int i = 0; i < 8; i += 2) {
+      const float2 y = add2s(mul2(make_float2(x[i], x[i + 1]), r), k);
+      b[i] = __float_as_uint(y.x);
+      b[i + 1] = __float_as_uint(y.y);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      b[i] = __float_as_uint(__fadd_rn(fminf(fmaxf(__fdiv_rn(x[i], q.s), -127.f), 127.f), 12582912.f));
   }
+  return make_uint2(low_bytes(b[0], b[1], b[2], b[3]), low_bytes(b[4], b[5], b[6], b[7]));
+}
+
+// 8 uint8 codes (v' >= 0); same reasoning, range [0, 255]
+__device__ __forceinline__ uint2 codes_uint8(const float* x, const QScale& q) {
+  if (q.mode == 0) return make_uint2(0u, 0u);
+  uint32_t b[8];
+  if (q.mode == 1) {
+    const float2 r = dup(q.r), k = dup(8388608.f);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const float2 y = add2s(mul2(make_float2(x[i], x[i + 1]), r), k);
+      b[i] = __float_as_uint(y.x);
+      b[i + 1] = __float_as_uint(y.y);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      b[i] = __float_as_uint(__fadd_rn(fminf(fmaxf(__fdiv_rn(x[i], q.s), 0.f), 255.f), 8388608.f));
+  }
+  return make_uint2(low_bytes(b[0], b[1], b[2], b[3]), low_bytes(b[4], b[5], b[6], b[7]));
+}
+
+// 8 E4M3 codes (round to nearest even, saturating); scale 0 keeps each sign
+__device__ __forceinline__ uint2 codes_e4m3(const float* x, const QScale& q) {
+  uint32_t w[4];
+  if (q.mode == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = ((__float_as_uint(x[2 * i]) >> 24) & 0x80u) | ((__float_as_uint(x[2 * i + 1]) >> 16) & 0x8000u);
+  } else if (q.mode == 1) {
+    const float2 r = dup(q.r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = uint32_t(__nv_cvt_float2_to_fp8x2(mul2(make_float2(x[2 * i], x[2 * i + 1]), r), __NV_SATFINITE, __NV_E4M3));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = uint32_t(__nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(x[2 * i], q.s), __fdiv_rn(x[2 * i + 1], q.s)),
+                                               __NV_SATFINITE, __NV_E4M3));
+  }
+  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
 __device__ __forceinline__ void store_p8(float* dst, const float* p) {
   reinterpret_cast<float4*>(dst)[0] = make_float4(p[0], p[1], p[2], p[3]);
   reinterpret_cast<float4*>(dst)[1] = make_float4(p[4], p[5], p[6], p[7]);
-}
-
-__device__ __forceinline__ uint2 pack_bytes(const uint32_t* b) {
-  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
 
 // ---------------------------------------------------------------- pack
@@ -195,21 +255,141 @@ __global__ void __launch_bounds__(kThreads) k_pack(const PackPiece* __restrict__
   }
 }
 
-// ---------------------------------------------------------------- Adam over one 8-element lane slice
-// Computes p', m', v' for the lane's n valid elements (n <= 8) and returns the
-// lane's partial absmax of m', v' and |p'| (as fp32 bits).
+// ---------------------------------------------------------------- asynchronous staging
+// A warp streams its Adam blocks through a few shared-memory stages filled with
+// cp.async, so that several blocks' loads are in flight per warp with few
+// registers.  Each lane reads back only the bytes it copied itself.
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// one stage of one warp: the 8-element slices of 32 lanes, lane-contiguous
+struct StageBuf {
+  uint4 g[32];
+  float4 p0[32], p1[32];
+  uint2 m[32], v[32];
+  float sc[4];  // the block's m and v scales (staged by lanes 0 and 1)
+};
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// lanes 0 and 1 stage the block's two scales
+__device__ __forceinline__ void stage_scales(StageBuf& sb, int lane, const AdamArgs& a, int slot) {
+  if (lane == 0) cp_async4(&sb.sc[0], a.m_scale + slot);
+  if (lane == 1) cp_async4(&sb.sc[1], a.v_scale + slot);
+}
+
+__device__ __forceinline__ uint32_t fastdiv(uint32_t n, uint32_t mul, uint32_t shr) {
+  return mul ? (__umulhi(n, mul) >> shr) : n;
+}
+
+__device__ __forceinline__ void stage_issue(StageBuf& sb, int lane, const AdamArgs& a, int64_t pos) {
+  cp_async16(&sb.g[lane], a.grad + pos);
+  cp_async16(&sb.p0[lane], a.master + pos);
+  cp_async16(&sb.p1[lane], a.master + pos + 4);
+  cp_async8(&sb.m[lane], a.m + pos);
+  cp_async8(&sb.v[lane], a.v + pos);
+}
+
+constexpr int kStages = 3;
+
+// ---------------------------------------------------------------- Adam over one 8-element lane slice
+// The lane's inputs stay packed (bf16 pairs, fp32 quads, code bytes) and are
+// unpacked element by element, which keeps the live register set small.
+
+struct Raw8 {
+  uint4 g;
+  float4 p0, p1;
+  uint2 m, v;
+};
+
+__device__ __forceinline__ Raw8 raw_from_stage(const StageBuf& sb, int lane) {
+  Raw8 r;
+  r.g = sb.g[lane];
+  r.p0 = sb.p0[lane];
+  r.p1 = sb.p1[lane];
+  r.m = sb.m[lane];
+  r.v = sb.v[lane];
+  return r;
+}
+
+__device__ __forceinline__ Raw8 raw_from_global(const AdamArgs& a, int64_t pos, int n) {
+  Raw8 r;
+  if (n == 8) {
+    r.g = *reinterpret_cast<const uint4*>(a.grad + pos);
+    r.p0 = *reinterpret_cast<const float4*>(a.master + pos);
+    r.p1 = *reinterpret_cast<const float4*>(a.master + pos + 4);
+    r.m = *reinterpret_cast<const uint2*>(a.m + pos);
+    r.v = *reinterpret_cast<const uint2*>(a.v + pos);
+    return r;
+  }
+  uint32_t g[4] = {0, 0, 0, 0}, m[2] = {0, 0}, v[2] = {0, 0};
+  float p[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < n) {
+      g[i >> 1] |= uint32_t(a.grad[pos + i]) << (16 * (i & 1));
+      p[i] = a.master[pos + i];
+      m[i >> 2] |= uint32_t(uint8_t(a.m[pos + i])) << (8 * (i & 3));
+      v[i >> 2] |= uint32_t(a.v[pos + i]) << (8 * (i & 3));
+    }
+  r.g = make_uint4(g[0], g[1], g[2], g[3]);
+  r.p0 = make_float4(p[0], p[1], p[2], p[3]);
+  r.p1 = make_float4(p[4], p[5], p[6], p[7]);
+  r.m = make_uint2(m[0], m[1]);
+  r.v = make_uint2(v[0], v[1]);
+  return r;
+}
+
+// Computes p', m', v' for the lane's n valid elements (n <= 8) and the lane's
+// partial maxima of |m'|, v' and |p'| (as fp32 bits).
 struct Lane8 {
   float p1[8], m1[8], v1[8];
   uint32_t am, av, ap;
 };
 
-__device__ __forceinline__ void adam_lane(const Hp& h, const Vec8& x, int n, float sm, float sv, Lane8& o) {
+template <bool FULL>
+__device__ __forceinline__ void adam_raw(const Hp& h, const Raw8& x, int n, float sm, float sv, Lane8& o) {
   o.am = o.av = o.ap = 0u;
+  const uint32_t gw[4] = {x.g.x, x.g.y, x.g.z, x.g.w};
+  const float pv[8] = {x.p0.x, x.p0.y, x.p0.z, x.p0.w, x.p1.x, x.p1.y, x.p1.z, x.p1.w};
+  const uint32_t mw[2] = {x.m.x ^ 0x80808080u, x.m.y ^ 0x80808080u}, vw[2] = {x.v.x, x.v.y};
+  const float2 sm2 = dup(sm), sv2 = dup(sv);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 g = make_float2(__uint_as_float(gw[j] << 16), __uint_as_float(gw[j] & 0xFFFF0000u));
+    const float2 qm = byte_pair(mw[j >> 1], 2 * (j & 1), 8388736.f);  // 2^23 + 128 for the flipped sign bit
+    const float2 qv = byte_pair(vw[j >> 1], 2 * (j & 1), 8388608.f);
+    float2 p1, m1, v1;
+    adam_pair(h, g, make_float2(pv[2 * j], pv[2 * j + 1]), qm, qv, sm2, sv2, p1, m1, v1);
+    o.p1[2 * j] = p1.x;
+    o.p1[2 * j + 1] = p1.y;
+    o.m1[2 * j] = m1.x;
+    o.m1[2 * j + 1] = m1.y;
+    o.v1[2 * j] = v1.x;
+    o.v1[2 * j + 1] = v1.y;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    adam_elem(h, x.g[i], x.p[i], x.qm[i], x.qv[i], sm, sv, o.p1[i], o.m1[i], o.v1[i]);
-    if (i < n) {
+    if (FULL || i < n) {
       o.am = max(o.am, __float_as_uint(fabsf(o.m1[i])));
       o.av = max(o.av, __float_as_uint(o.v1[i]));
       o.ap = max(o.ap, __float_as_uint(fabsf(o.p1[i])));
@@ -217,27 +397,41 @@ __device__ __forceinline__ void adam_lane(const Hp& h, const Vec8& x, int n, flo
   }
 }
 
-__device__ __forceinline__ void store_state(const AdamArgs& a, int64_t pos, int n, const Lane8& o, float smn,
-                                            float svn) {
-  uint32_t bm[8], bv[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    bm[i] = q_int8(o.m1[i], smn);
-    bv[i] = q_uint8(o.v1[i], svn);
-  }
+// Block scales of m' and v' from the lanes' partial maxima: lane 0 computes the
+// m scale, lane 1 the v scale (in parallel), everyone receives both.
+__device__ __forceinline__ void warp_block_scales(uint32_t am, uint32_t av, int lane, QScale& qm, QScale& qv) {
+  const uint32_t m_all = __reduce_max_sync(0xFFFFFFFFu, am);
+  const uint32_t v_all = __reduce_max_sync(0xFFFFFFFFu, av);
+  const QScale q = qscale(lane == 0 ? m_all : v_all, lane == 0 ? 127.f : 255.f);
+  qm.s = __shfl_sync(0xFFFFFFFFu, q.s, 0);
+  qm.r = __shfl_sync(0xFFFFFFFFu, q.r, 0);
+  qm.mode = __shfl_sync(0xFFFFFFFFu, q.mode, 0);
+  qv.s = __shfl_sync(0xFFFFFFFFu, q.s, 1);
+  qv.r = __shfl_sync(0xFFFFFFFFu, q.r, 1);
+  qv.mode = __shfl_sync(0xFFFFFFFFu, q.mode, 1);
+}
+
+__device__ __forceinline__ void store_bytes(uint8_t* dst, uint2 w, int n) {
   if (n == 8) {
-    store_p8(a.master + pos, o.p1);
-    *reinterpret_cast<uint2*>(a.m + pos) = pack_bytes(bm);
-    *reinterpret_cast<uint2*>(a.v + pos) = pack_bytes(bv);
+    *reinterpret_cast<uint2*>(dst) = w;
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (i < n) {
-        a.master[pos + i] = o.p1[i];
-        a.m[pos + i] = int8_t(bm[i]);
-        a.v[pos + i] = uint8_t(bv[i]);
-      }
+      if (i < n) dst[i] = uint8_t(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFFu);
   }
+}
+
+__device__ __forceinline__ void store_state(const AdamArgs& a, int64_t pos, int n, const Lane8& o, const QScale& qm,
+                                            const QScale& qv) {
+  if (n == 8) {
+    store_p8(a.master + pos, o.p1);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < n) a.master[pos + i] = o.p1[i];
+  }
+  store_bytes(reinterpret_cast<uint8_t*>(a.m) + pos, codes_int8(o.m1, qm), n);
+  store_bytes(a.v + pos, codes_uint8(o.v1, qv), n);
 }
 
 // ---------------------------------------------------------------- flat blocks (1-D / no 2-D FP8)
@@ -246,53 +440,38 @@ __device__ __forceinline__ void store_state(const AdamArgs& a, int64_t pos, int 
 // E = 4: 128-element blocks (FP8 tile = the block).
 
 template <int E>
-__global__ void __launch_bounds__(kThreads) k_flat(const FlatGroup* __restrict__ groups, AdamArgs a) {
+__global__ void __launch_bounds__(kThreads, kAdamCtas) k_flat(const FlatGroup* __restrict__ groups, AdamArgs a) {
   constexpr int B = 32 * E;
   const FlatGroup g = groups[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Hp h{a.hp.lr, a.hp.b1, a.hp.b2, a.hp.eps, a.hp.omb1, a.hp.omb2, a.hp.bc1, a.hp.bc2};
+  const Hp h = make_hp(a.hp);
   const int nblk = (g.nelem + B - 1) / B;
   const bool do_fp8 = a.fp8 != nullptr && g.fslot >= 0;
   for (int b = warp; b < nblk; b += kWarps) {
-    const int e0 = b * B + lane * E;         // element offset in the group
+    const int e0 = b * B + lane * E;             // element offset in the group
     const int n = max(0, min(E, g.nelem - e0));  // valid elements of this lane
     const int64_t pos = g.pos + e0;
-    Vec8 x;
-    if (E == 8 && n == 8) {
-      load8(a, pos, x);
-    } else {
-      load_tail(a, pos, n, x);
-    }
+    const Raw8 x = raw_from_global(a, pos, n);
     const int slot = g.mslot + b;
     const float sm = a.m_scale[slot], sv = a.v_scale[slot];
     Lane8 o;
-    adam_lane(h, x, n, sm, sv, o);
-    const uint32_t am = __reduce_max_sync(0xFFFFFFFFu, o.am);
-    const uint32_t av = __reduce_max_sync(0xFFFFFFFFu, o.av);
-    const float smn = scale_of(am, 127.f), svn = scale_of(av, 255.f);
-    store_state(a, pos, n, o, smn, svn);
+    if (n == 8) adam_raw<true>(h, x, n, sm, sv, o);
+    else adam_raw<false>(h, x, n, sm, sv, o);
+    QScale qm, qv;
+    warp_block_scales(o.am, o.av, lane, qm, qv);
+    store_state(a, pos, n, o, qm, qv);
     if (lane == 0) {
-      a.m_scale[slot] = smn;
-      a.v_scale[slot] = svn;
+      a.m_scale[slot] = qm.s;
+      a.v_scale[slot] = qv.s;
     }
     if (do_fp8) {
       uint32_t ap = o.ap;
       // reduce over the lanes of one 128-element tile: 16 lanes (E = 8) or 32 (E = 4)
 #pragma unroll
       for (int off = (E == 8 ? 8 : 16); off >= 1; off >>= 1) ap = max(ap, __shfl_xor_sync(0xFFFFFFFFu, ap, off));
-      const float s = scale_of(ap, 448.f);
-      uint32_t q[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = q_e4m3(o.p1[i], s);
-      if (E == 8 && n == 8) {
-        *reinterpret_cast<uint2*>(a.fp8 + pos) = pack_bytes(q);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < n) a.fp8[pos + i] = uint8_t(q[i]);
-      }
-      const int tile_first = (e0 / 128) * 128;  // first element of this lane's tile
-      if (e0 == tile_first && tile_first < g.nelem) a.fp8_scale[g.fslot + e0 / 128] = s;
+      const QScale qp = qscale(ap, 448.f);
+      store_bytes(a.fp8 + pos, codes_e4m3(o.p1, qp), n);
+      if ((e0 & 127) == 0 && e0 < g.nelem) a.fp8_scale[g.fslot + e0 / 128] = qp.s;
     }
   }
 }
@@ -302,15 +481,22 @@ __global__ void __launch_bounds__(kThreads) k_flat(const FlatGroup* __restrict__
 // 256-element blocks, write state and master, and fold |p'| into per-column-tile
 // maxima in shared memory.  Phase 2: tile scales, then the updated master is
 // re-read (it was written moments ago by this CTA and is served from L2) and
-// converted to E4M3.
+// converted to E4M3.  Shared memory: 2 words per column tile.
 
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads) k_strip(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
-  extern __shared__ uint32_t s_tile[];
+__global__ void __launch_bounds__(kThreads, kAdamCtas) k_strip(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
+  // dynamic shared memory: the warps' staging pipes, then 2 words per FP8
+  // column tile ([ntile] amax bits, later r; [ntile..2*ntile) s)
+  extern __shared__ __align__(16) unsigned char s_dyn[];
+  StageBuf* pipe = reinterpret_cast<StageBuf*>(s_dyn);
+  uint32_t* s_tile = reinterpret_cast<uint32_t*>(s_dyn + sizeof(StageBuf) * kWarps * kStages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Hp h{a.hp.lr, a.hp.b1, a.hp.b2, a.hp.eps, a.hp.omb1, a.hp.omb2, a.hp.bc1, a.hp.bc2};
+  const Hp h = make_hp(a.hp);
+  StageBuf* st = pipe + warp * kStages;
   for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
     const RegionGroup g = groups[gi];
+    // strip: rows x 256 columns, block = one row segment; band: rows x C,
+    // flat 256-element blocks from the band start
     const bool flat = g.width == g.C;
     const int ntile = (g.width + 127) >> 7;
     if (FP8) {
@@ -318,73 +504,117 @@ __global__ void __launch_bounds__(kThreads) k_strip(const RegionGroup* __restric
       __syncthreads();
     }
     const int nel = g.rows * g.width;
-    const int nblk = (nel + 255) >> 8;
-    const int bpr = g.width >> 8;  // blocks per row (strip mode)
-    for (int b = warp; b < nblk; b += kWarps) {
-      int off, slot, col;
-      if (flat) {
-        off = b << 8;
-        slot = g.mslot + b;
-        col = (off + lane * 8) % g.C;
-      } else {
-        const int r = b / bpr, j = b - r * bpr;
-        off = r * g.C + (j << 8);
-        slot = g.mslot + r * (g.C >> 8) + j;
-        col = (j << 8) + lane * 8;
+    const int nblk = flat ? (nel + 255) >> 8 : g.rows;
+    const int rstep = g.C >> 8;  // strip: slots per row
+    // geometry of this warp's k-th block: lane position, valid count, slot
+    auto geom = [&](int k, int64_t& pos, int& n, int& slot) {
+      const int b = warp + k * kWarps;
+      const int off = flat ? (b << 8) : b * g.C;
+      slot = g.mslot + (flat ? b : b * rstep);
+      n = flat ? max(0, min(8, nel - off - lane * 8)) : 8;
+      pos = g.pos + off + lane * 8;
+    };
+    const int nb_w = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
+#pragma unroll
+    for (int k = 0; k < kStages - 1; ++k) {
+      if (k < nb_w) {
+        int64_t pos; int n, slot;
+        geom(k, pos, n, slot);
+        if (n == 8) stage_issue(st[k], lane, a, pos);
+        stage_scales(st[k], lane, a, slot);
       }
-      const int n = flat ? max(0, min(8, nel - off - lane * 8)) : 8;
-      const int64_t pos = g.pos + off + lane * 8;
-      Vec8 x;
-      if (n == 8) load8(a, pos, x);
-      else load_tail(a, pos, n, x);
-      const float sm = a.m_scale[slot], sv = a.v_scale[slot];
+      cp_async_commit();
+    }
+    for (int k = 0; k < nb_w; ++k) {
+      const int kn = k + kStages - 1;
+      __syncwarp();
+      if (kn < nb_w) {
+        int64_t pos; int n, slot;
+        geom(kn, pos, n, slot);
+        if (n == 8) stage_issue(st[kn % kStages], lane, a, pos);
+        stage_scales(st[kn % kStages], lane, a, slot);
+      }
+      cp_async_commit();
+      cp_async_wait<kStages - 1>();
+      __syncwarp();  // lanes 0 and 1 staged the scales every lane reads
+      int64_t pos; int n, slot;
+      geom(k, pos, n, slot);
+      const StageBuf& sb = st[k % kStages];
+      const Raw8 x = n == 8 ? raw_from_stage(sb, lane) : raw_from_global(a, pos, n);
       Lane8 o;
-      adam_lane(h, x, n, sm, sv, o);
-      const uint32_t am = __reduce_max_sync(0xFFFFFFFFu, o.am);
-      const uint32_t av = __reduce_max_sync(0xFFFFFFFFu, o.av);
-      const float smn = scale_of(am, 127.f), svn = scale_of(av, 255.f);
-      store_state(a, pos, n, o, smn, svn);
+      if (n == 8) adam_raw<true>(h, x, n, sb.sc[0], sb.sc[1], o);
+      else adam_raw<false>(h, x, n, sb.sc[0], sb.sc[1], o);
+      QScale qm, qv;
+      warp_block_scales(o.am, o.av, lane, qm, qv);
+      store_state(a, pos, n, o, qm, qv);
       if (lane == 0) {
-        a.m_scale[slot] = smn;
-        a.v_scale[slot] = svn;
+        a.m_scale[slot] = qm.s;
+        a.v_scale[slot] = qv.s;
       }
       if (FP8) {
-        const int t = col >> 7;
-        const unsigned same = __match_any_sync(0xFFFFFFFFu, t);
-        const uint32_t ap = __reduce_max_sync(same, o.ap);
-        if (lane == __ffs(same) - 1) atomicMax(&s_tile[t], ap);
+        if (flat) {
+          // column of the lane's first element; several lanes share a tile
+          const int b = warp + k * kWarps;
+          const uint32_t e = uint32_t((b << 8) + lane * 8);
+          const int col = int(e - fastdiv(e, g.cmul, g.cshr) * uint32_t(g.C));
+          const int t = col >> 7;
+          const unsigned same = __match_any_sync(0xFFFFFFFFu, t);
+          const uint32_t ap = __reduce_max_sync(same, o.ap);
+          if (lane == __ffs(same) - 1) atomicMax(&s_tile[t], ap);
+        } else {
+          // strip: lanes 0-15 cover tile 0, lanes 16-31 tile 1
+          uint32_t ap = o.ap;
+#pragma unroll
+          for (int off = 8; off >= 1; off >>= 1) ap = max(ap, __shfl_xor_sync(0xFFFFFFFFu, ap, off));
+          if ((lane & 15) == 0) atomicMax(&s_tile[lane >> 4], ap);
+        }
       }
     }
+    cp_async_wait<0>();
     if (FP8) {
       __syncthreads();
       for (int t = threadIdx.x; t < ntile; t += kThreads) {
-        const float s = scale_of(s_tile[t], 448.f);
-        a.fp8_scale[g.fslot + t] = s;
-        s_tile[t] = __float_as_uint(s);
+        const QScale q = qscale(s_tile[t], 448.f);
+        a.fp8_scale[g.fslot + t] = q.s;
+        s_tile[t] = __float_as_uint(q.r);
+        s_tile[ntile + t] = __float_as_uint(q.s);
       }
       __syncthreads();
       const int nvec = nel >> 3;
-      const int vpr = g.width >> 3;
-      for (int v = threadIdx.x; v < nvec; v += kThreads) {
-        int64_t pos;
-        int col;
-        if (flat) {
-          const int e = v << 3;
-          col = e % g.C;
-          pos = g.pos + e;
-        } else {
-          const int r = v / vpr, k = v - r * vpr;
-          col = k << 3;
-          pos = g.pos + int64_t(r) * g.C + col;
-        }
-        const float s = __uint_as_float(s_tile[col >> 7]);
-        const float4 p0 = *reinterpret_cast<const float4*>(a.master + pos);
-        const float4 p1 = *reinterpret_cast<const float4*>(a.master + pos + 4);
-        const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        uint32_t q[8];
+      constexpr int U = 2;
+      for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * U) {
+        float4 p0[U], p1[U];
+        int64_t pos[U];
+        int tile[U];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = q_e4m3(pv[i], s);
-        *reinterpret_cast<uint2*>(a.fp8 + pos) = pack_bytes(q);
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * kThreads;
+          if (v < nvec) {
+            if (flat) {
+              const uint32_t e = uint32_t(v) << 3;
+              tile[u] = int(e - fastdiv(e, g.cmul, g.cshr) * uint32_t(g.C)) >> 7;
+              pos[u] = g.pos + e;
+            } else {
+              const int r = v >> 5, kk = v & 31;  // 32 vectors of 8 per 256-column row
+              tile[u] = kk >> 4;
+              pos[u] = g.pos + int64_t(r) * g.C + (kk << 3);
+            }
+            p0[u] = *reinterpret_cast<const float4*>(a.master + pos[u]);
+            p1[u] = *reinterpret_cast<const float4*>(a.master + pos[u] + 4);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * kThreads;
+          if (v < nvec) {
+            QScale q;
+            q.r = __uint_as_float(s_tile[tile[u]]);
+            q.s = __uint_as_float(s_tile[ntile + tile[u]]);
+            q.mode = q.s == 0.f ? 0 : (isinf(q.r) ? 2 : 1);
+            const float pv[8] = {p0[u].x, p0[u].y, p0[u].z, p0[u].w, p1[u].x, p1[u].y, p1[u].z, p1[u].w};
+            *reinterpret_cast<uint2*>(a.fp8 + pos[u]) = codes_e4m3(pv, q);
+          }
+        }
       }
       __syncthreads();  // s_tile is reused by the next region
     }
@@ -396,16 +626,15 @@ __global__ void __launch_bounds__(kThreads) k_strip(const RegionGroup* __restric
 // Phase 2: requantise m', v' (recomputed from the untouched old codes and the
 // old scales held in registers, bit-identical) and convert p' (re-read, L2).
 
-__device__ __forceinline__ uint32_t block_max(uint32_t x, uint32_t* red, int which) {
+__device__ __forceinline__ void block_max(uint32_t x, uint32_t* red, int which) {
   x = __reduce_max_sync(0xFFFFFFFFu, x);
   if ((threadIdx.x & 31) == 0) red[which * kWarps + (threadIdx.x >> 5)] = x;
-  return x;
 }
 
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads) k_tile(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
+__global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
   __shared__ uint32_t red[3 * kWarps];
-  const Hp h{a.hp.lr, a.hp.b1, a.hp.b2, a.hp.eps, a.hp.omb1, a.hp.omb2, a.hp.bc1, a.hp.bc2};
+  const Hp h = make_hp(a.hp);
   for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
     const RegionGroup g = groups[gi];
     const bool fp8 = FP8 && g.fslot >= 0;
@@ -415,10 +644,9 @@ __global__ void __launch_bounds__(kThreads) k_tile(const RegionGroup* __restrict
     for (int v = threadIdx.x; v < nvec; v += kThreads) {
       const int r = v / vpr, k = v - r * vpr;
       const int64_t pos = g.pos + int64_t(r) * g.C + (k << 3);
-      Vec8 x;
-      load8(a, pos, x);
+      const Raw8 x = raw_from_global(a, pos, 8);
       Lane8 o;
-      adam_lane(h, x, 8, sm, sv, o);
+      adam_raw<true>(h, x, 8, sm, sv, o);
       store_p8(a.master + pos, o.p1);
       am = max(am, o.am);
       av = max(av, o.av);
@@ -435,32 +663,23 @@ __global__ void __launch_bounds__(kThreads) k_tile(const RegionGroup* __restrict
       tv = max(tv, red[kWarps + w]);
       tp = max(tp, red[2 * kWarps + w]);
     }
-    const float smn = scale_of(tm, 127.f), svn = scale_of(tv, 255.f), sp = scale_of(tp, 448.f);
+    const QScale qm = qscale(tm, 127.f), qv = qscale(tv, 255.f), qp = qscale(tp, 448.f);
     if (threadIdx.x == 0) {
-      a.m_scale[g.mslot] = smn;
-      a.v_scale[g.mslot] = svn;
-      if (fp8) a.fp8_scale[g.fslot] = sp;
+      a.m_scale[g.mslot] = qm.s;
+      a.v_scale[g.mslot] = qv.s;
+      if (fp8) a.fp8_scale[g.fslot] = qp.s;
     }
     for (int v = threadIdx.x; v < nvec; v += kThreads) {
       const int r = v / vpr, k = v - r * vpr;
       const int64_t pos = g.pos + int64_t(r) * g.C + (k << 3);
-      Vec8 x;
-      load8(a, pos, x);  // old codes; x.p now holds p' (unused for the state)
+      const Raw8 x = raw_from_global(a, pos, 8);  // old codes; the master words now hold p'
       Lane8 o;
-      adam_lane(h, x, 8, sm, sv, o);
-      uint32_t bm[8], bv[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        bm[i] = q_int8(o.m1[i], smn);
-        bv[i] = q_uint8(o.v1[i], svn);
-      }
-      *reinterpret_cast<uint2*>(a.m + pos) = pack_bytes(bm);
-      *reinterpret_cast<uint2*>(a.v + pos) = pack_bytes(bv);
+      adam_raw<true>(h, x, 8, sm, sv, o);
+      *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);
+      *reinterpret_cast<uint2*>(a.v + pos) = codes_uint8(o.v1, qv);
       if (fp8) {
-        uint32_t q[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = q_e4m3(x.p[i], sp);
-        *reinterpret_cast<uint2*>(a.fp8 + pos) = pack_bytes(q);
+        const float pv[8] = {x.p0.x, x.p0.y, x.p0.z, x.p0.w, x.p1.x, x.p1.y, x.p1.z, x.p1.w};
+        *reinterpret_cast<uint2*>(a.fp8 + pos) = codes_e4m3(pv, qp);
       }
     }
     __syncthreads();  // red is reused by the next tile
@@ -495,25 +714,16 @@ __global__ void __launch_bounds__(kThreads) k_quant_flat(const FlatGroup* __rest
       if (i < n) ap = max(ap, __float_as_uint(fabsf(p[i])));
 #pragma unroll
     for (int off = 8; off >= 1; off >>= 1) ap = max(ap, __shfl_xor_sync(0xFFFFFFFFu, ap, off));
-    const float s = scale_of(ap, 448.f);
-    uint32_t q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = q_e4m3(p[i], s);
-    if (n == 8) {
-      *reinterpret_cast<uint2*>(fp8 + pos) = pack_bytes(q);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i < n) fp8[pos + i] = uint8_t(q[i]);
-    }
-    if ((e0 & 127) == 0 && e0 < g.nelem) fp8_scale[g.fslot + e0 / 128] = s;
+    const QScale q = qscale(ap, 448.f);
+    store_bytes(fp8 + pos, codes_e4m3(p, q), n);
+    if ((e0 & 127) == 0 && e0 < g.nelem) fp8_scale[g.fslot + e0 / 128] = q.s;
   }
 }
 
 __global__ void __launch_bounds__(kThreads) k_quant_region(const RegionGroup* __restrict__ groups, int ngroups,
                                                            const float* __restrict__ master,
                                                            uint8_t* __restrict__ fp8, float* __restrict__ fp8_scale) {
-  extern __shared__ uint32_t s_tile[];
+  extern __shared__ uint32_t s_tile[];  // [ntile] amax bits, later r; [ntile..2*ntile) s
   for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
     const RegionGroup g = groups[gi];
     if (g.fslot < 0) continue;  // uniform per CTA
@@ -543,19 +753,20 @@ __global__ void __launch_bounds__(kThreads) k_quant_region(const RegionGroup* __
           for (int i = 0; i < 8; ++i) ap = max(ap, __float_as_uint(fabsf(pv[i])));
           atomicMax(&s_tile[col >> 7], ap);
         } else {
-          const float s = __uint_as_float(s_tile[col >> 7]);
-          uint32_t q[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) q[i] = q_e4m3(pv[i], s);
-          *reinterpret_cast<uint2*>(fp8 + pos) = pack_bytes(q);
+          QScale q;
+          q.r = __uint_as_float(s_tile[col >> 7]);
+          q.s = __uint_as_float(s_tile[ntile + (col >> 7)]);
+          q.mode = q.s == 0.f ? 0 : (isinf(q.r) ? 2 : 1);
+          *reinterpret_cast<uint2*>(fp8 + pos) = codes_e4m3(pv, q);
         }
       }
       __syncthreads();
       if (pass == 0) {
         for (int t = threadIdx.x; t < ntile; t += kThreads) {
-          const float s = scale_of(s_tile[t], 448.f);
-          fp8_scale[g.fslot + t] = s;
-          s_tile[t] = __float_as_uint(s);
+          const QScale q = qscale(s_tile[t], 448.f);
+          fp8_scale[g.fslot + t] = q.s;
+          s_tile[t] = __float_as_uint(q.r);
+          s_tile[ntile + t] = __float_as_uint(q.s);
         }
         __syncthreads();
       }
@@ -569,9 +780,9 @@ int check_launch(const char* what) {
   return BQ_OK;
 }
 
-constexpr int kStripCtasPerSm = 2;
-constexpr int kTileCtasPerSm = 2;
-constexpr int kMaxStripTiles = 12288;  // 48 KB of shared memory
+constexpr int kStripCtasPerSm = kAdamCtas;
+constexpr int kTileCtasPerSm = kAdamCtas;
+constexpr int kMaxStripTiles = 6144;  // 2 words per tile: 48 KB of shared memory
 
 }  // namespace
 
@@ -600,11 +811,17 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
   }
   if (t.n_strips) {
     const int grid = std::min(t.n_strips, sms * kStripCtasPerSm);
-    const size_t smem = size_t(t.max_strip_tiles) * sizeof(uint32_t);
+    const size_t smem = sizeof(StageBuf) * kWarps * kStages + 2 * size_t(t.max_strip_tiles) * sizeof(uint32_t);
+    static bool attr_done = false;
+    if (!attr_done) {
+      cudaFuncSetAttribute(k_strip<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaFuncSetAttribute(k_strip<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      attr_done = true;
+    }
     if (fp8)
       k_strip<true><<<grid, kThreads, smem, s>>>(t.strips, t.n_strips, a);
     else
-      k_strip<false><<<grid, kThreads, 0, s>>>(t.strips, t.n_strips, a);
+      k_strip<false><<<grid, kThreads, smem, s>>>(t.strips, t.n_strips, a);
     if (int rc = check_launch("bq_step_adam8 (strips)")) return rc;
   }
   if (t.n_tiles) {
@@ -631,13 +848,13 @@ int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, floa
     if (int rc = check_launch("bq_quant_fp8 (flat128)")) return rc;
   }
   if (t.n_strips) {
-    const size_t smem = size_t(std::max(t.max_strip_tiles, 1)) * sizeof(uint32_t);
+    const size_t smem = 2 * size_t(std::max(t.max_strip_tiles, 1)) * sizeof(uint32_t);
     k_quant_region<<<std::min(t.n_strips, sms * kStripCtasPerSm), kThreads, smem, s>>>(t.strips, t.n_strips, master,
                                                                                         fp8, fp8_scale);
     if (int rc = check_launch("bq_quant_fp8 (strips)")) return rc;
   }
   if (t.n_tiles) {
-    k_quant_region<<<std::min(t.n_tiles, sms * kTileCtasPerSm), kThreads, sizeof(uint32_t), s>>>(
+    k_quant_region<<<std::min(t.n_tiles, sms * kTileCtasPerSm), kThreads, 2 * sizeof(uint32_t), s>>>(
         t.tiles, t.n_tiles, master, fp8, fp8_scale);
     if (int rc = check_launch("bq_quant_fp8 (tiles)")) return rc;
   }

@@ -84,10 +84,11 @@ typedef struct {
   int64_t case3_prefix;  /* length of the winning Case-3 prefix */
 } bq_layout_info;
 
-/* fp32 Adam hyper-parameters; omb1 = 1-b1, omb2 = 1-b2, bc1 = 1-b1^t and
- * bc2 = 1-b2^t are supplied by the caller (computed in fp64, rounded once). */
+/* fp32 Adam hyper-parameters; omb1 = 1-b1, omb2 = 1-b2 and the reciprocal bias
+ * corrections rbc1 = 1/(1-b1^t), rbc2 = 1/(1-b2^t) are supplied by the caller
+ * (computed in fp64, rounded once to fp32). */
 typedef struct {
-  float lr, b1, b2, eps, omb1, omb2, bc1, bc2;
+  float lr, b1, b2, eps, omb1, omb2, rbc1, rbc2;
 } bq_adam_hp;
 
 /* One Newton-Schulz problem: bf16 row-major x (rows x cols, row pitch ld_x
@@ -165,11 +166,13 @@ int bq_pack(const bq_shard* shard, const void* const* grad_ptrs, void* dbuf_grad
  * paper section 6.3) and block-wise FP8 (DeepSeek-V3 style, bud-325 TL;DR).
  * Per element, each an IEEE fp32 op rounded to nearest, no FMA:
  *   g=f32(grad); m=qm*sm; v=qv*sv; m'=b1*m+omb1*g; v'=b2*v+omb2*(g*g);
- *   p'=p-lr*((m'/bc1)/(sqrt(v'/bc2)+eps))
- * per Adam block: sm'=max|m'|/127, qm'=clamp(rint(m'/sm'),-127,127);
- *   sv'=max v'/255, qv'=clamp(rint(v'/sv'),0,255); all-zero block -> scale 0.
- * per FP8 tile (if fp8_out != NULL): s=max|p'|/448, code=e4m3_rne_satfinite(p'/s);
- *   all-zero tile -> s=0, codes +-0.
+ *   p'=p-lr*((m'*rbc1)/(sqrt(v'*rbc2)+eps))
+ * per Adam block: sm'=max|m'|/127, qm'=clamp(rint(m'*(127/max|m'|)),-127,127);
+ *   sv'=max v'/255, qv'=clamp(rint(v'*(255/max v')),0,255) (the reciprocal is
+ *   one fp32 division per block; if it overflows, m'/sm' resp. v'/sv' is used);
+ *   a block whose scale is 0 gets zero codes.
+ * per FP8 tile (if fp8_out != NULL): s=max|p'|/448, code=e4m3_rne_satfinite(
+ *   p'*(448/max|p'|)) (p'/s if the reciprocal overflows); scale 0 -> codes +-0.
  * grad: bf16 packed buffer; master fp32, m int8, v uint8, fp8_out uint8 - all
  * (dev_hi-dev_lo)*S elements, updated in place (padding untouched); m_scale,
  * v_scale: fp32 per Adam slot; fp8_scale: fp32 per FP8 slot (a scale buffer may

@@ -18,10 +18,11 @@ Readings (the pages give neither the update nor the quantiser):
         g   = f32(bf16 grad)
         m   = code_m * s_m            v   = code_v * s_v
         m'  = b1*m + omb1*g           v'  = b2*v + omb2*(g*g)
-        mh  = m' / bc1                vh  = v' / bc2
+        mh  = m' * rbc1               vh  = v' * rbc2
         p'  = p - lr * (mh / (sqrt(vh) + eps))
-    with omb1 = 1-b1, omb2 = 1-b2, bc1 = 1-b1^t, bc2 = 1-b2^t evaluated in fp64
-    and rounded once to fp32 (adam_hparams);
+    with omb1 = 1-b1, omb2 = 1-b2 and the reciprocal bias corrections
+    rbc1 = 1/(1-b1^t), rbc2 = 1/(1-b2^t) evaluated in fp64 and rounded once to
+    fp32 (adam_hparams);
   * a block is 256 consecutive elements of the tensor (the last one may be short),
     or a 128x128 tile of the tensor's 2-D view (1-D tensors: 128 elements).
 """
@@ -39,7 +40,7 @@ def adam_hparams(lr, b1, b2, eps, t):
     lr, b1, b2, eps = float(lr), float(b1), float(b2), float(eps)
     return dict(lr=F32(lr), b1=F32(b1), b2=F32(b2), eps=F32(eps),
                 omb1=F32(1.0 - b1), omb2=F32(1.0 - b2),
-                bc1=F32(1.0 - b1 ** t), bc2=F32(1.0 - b2 ** t))
+                rbc1=F32(1.0 / (1.0 - b1 ** t)), rbc2=F32(1.0 / (1.0 - b2 ** t)))
 
 
 def adam_update(g_bits, p, m, v, hp):
@@ -48,8 +49,8 @@ def adam_update(g_bits, p, m, v, hp):
     p = np.asarray(p, dtype=np.float32)
     m1 = hp["b1"] * m + hp["omb1"] * g
     v1 = hp["b2"] * v + hp["omb2"] * (g * g)
-    mh = m1 / hp["bc1"]
-    vh = v1 / hp["bc2"]
+    mh = m1 * hp["rbc1"]
+    vh = v1 * hp["rbc2"]
     p1 = p - hp["lr"] * (mh / (np.sqrt(vh) + hp["eps"]))
     return p1.astype(np.float32), m1.astype(np.float32), v1.astype(np.float32)
 

@@ -10,7 +10,8 @@
   from that definition, with round-to-nearest-even and saturation to +-448.
 * int8 / uint8 linear absmax block quantisers for the 8-bit Adam state ("8-bit
   Adam" in Key claims; the pages give block locality but no quantiser, so the
-  reading is a symmetric linear map with one fp32 absmax scale per block).
+  reading is a symmetric linear map with one fp32 absmax scale per block; codes
+  are formed by multiplying with the reciprocal scale, computed once per block).
 
 Everything is numpy; fp32 arithmetic is done on float32 arrays so that every
 operation is one IEEE fp32 operation rounded to nearest.
@@ -104,32 +105,54 @@ def e4m3_encode(x):
 # ----------------------------------------------------------------------------- linear absmax block quantisers
 
 
+def block_scale(amax, qmax):
+    """(stored scale s, reciprocal r, mode) of a block with absmax amax mapped to
+    qmax.  s = amax / qmax and r = qmax / amax, each one fp32 division.
+    mode 0: s == 0 (all-zero block, or amax so small that s underflows): codes 0;
+    mode 1: r finite: codes from x * r;
+    mode 2: r overflowed (amax below ~qmax / 3.4e38): codes from x / s."""
+    with np.errstate(over="ignore", divide="ignore"):
+        s = F32(amax) / F32(qmax)
+        r = F32(qmax) / F32(amax)
+    if s == 0:
+        return F32(0), r, 0
+    return F32(s), r, (1 if np.isfinite(r) else 2)
+
+
+def scaled(x, s, r, mode):
+    """x * r (mode 1) or x / s (mode 2), fp32."""
+    x = np.asarray(x, dtype=np.float32)
+    return x * r if mode == 1 else x / s
+
+
 def quant_int8_absmax(x):
     """One block of signed state -> (int8 codes, fp32 scale).
 
-    s = max|x| / 127 (fp32 division); code = clamp(rint(x / s), -127, 127) with
-    rint = half-to-even; an all-zero block gets s = 0 and zero codes.  -128 is
-    never produced (symmetric range)."""
+    s = max|x| / 127 is the stored scale; the codes use the reciprocal
+    r = 127 / max|x| (one fp32 division per block): code = clamp(rint(x * r),
+    -127, 127), rint = half-to-even (x / s when r overflows, see block_scale).
+    A block whose scale is 0 gets zero codes; -128 is never produced."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     amax = np.max(np.abs(x)) if x.size else F32(0)
-    if amax == 0:
+    s, r, mode = block_scale(amax, 127)
+    if mode == 0:
         return np.zeros(x.shape, np.int8), F32(0)
-    s = F32(amax) / F32(127)
-    q = np.clip(np.rint(x / s), -127, 127)
-    return q.astype(np.int8), F32(s)
+    q = np.clip(np.rint(scaled(x, s, r, mode)), -127, 127)
+    return q.astype(np.int8), s
 
 
 def quant_uint8_absmax(x):
     """One block of non-negative state -> (uint8 codes, fp32 scale).
 
-    s = max x / 255; code = clamp(rint(x / s), 0, 255); all-zero -> s = 0."""
+    s = max x / 255; code = clamp(rint(x * r), 0, 255) with r = 255 / max x
+    (x / s when r overflows); a block whose scale is 0 gets zero codes."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     amax = np.max(x) if x.size else F32(0)
-    if amax == 0:
+    s, r, mode = block_scale(amax, 255)
+    if mode == 0:
         return np.zeros(x.shape, np.uint8), F32(0)
-    s = F32(amax) / F32(255)
-    q = np.clip(np.rint(x / s), 0, 255)
-    return q.astype(np.uint8), F32(s)
+    q = np.clip(np.rint(scaled(x, s, r, mode)), 0, 255)
+    return q.astype(np.uint8), s
 
 
 def dequant(codes, scale):

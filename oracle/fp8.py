@@ -9,15 +9,17 @@ which is what RaggedShard's granularity guarantees.
 
 Readings (the pages give no formula): blocks are 128x128 tiles of the tensor's
 row-major 2-D view, clipped at the edges (1-D tensors: 1x128); per tile
-    amax = max |p'|,  s = amax / 448 (fp32 division),
-    code = e4m3(p' / s)  (fp32 division, then round-to-nearest-even, saturating),
-and an all-zero tile gets s = 0 with codes +0 / -0 following each element's sign.
+    amax = max |p'|,  s = amax / 448 (fp32 division, the stored scale),
+    r = 448 / amax (fp32 division, once per tile),
+    code = e4m3(p' * r)  (fp32 product, then round-to-nearest-even, saturating),
+(p' / s instead when r overflows, amax below ~1.3e-36), and a tile whose scale
+is 0 gets s = 0 with codes +0 / -0 following each element's sign.
 Codes go to the same local offsets as the parameters; s goes to the tile's slot.
 """
 
 import numpy as np
 
-from .codecs import e4m3_encode
+from .codecs import block_scale, e4m3_encode, scaled
 from .planner import fp8_tiles
 
 F32 = np.float32
@@ -27,10 +29,10 @@ def fp8_tile(p):
     """One tile -> (uint8 E4M3 codes, fp32 scale)."""
     p = np.ascontiguousarray(p, dtype=np.float32)
     amax = np.max(np.abs(p)) if p.size else F32(0)
-    if amax == 0:
-        return e4m3_encode(p), F32(0)  # +-0 -> 0x00 / 0x80
-    s = F32(amax) / F32(448)
-    return e4m3_encode(p / s), F32(s)
+    s, r, mode = block_scale(amax, 448)
+    if mode == 0:  # +-0 codes following each element's sign
+        return (p.view(np.uint32) >> 24).astype(np.uint8) & np.uint8(0x80), F32(0)
+    return e4m3_encode(scaled(p, s, r, mode)), s
 
 
 def quant_fp8(layout, dev_lo, dev_hi, master, fp8_out, fp8_scale, tiles=None):

@@ -167,3 +167,20 @@ def test_shard_tables_pass_host_bounds_check():
         for lo, hi in ranges:
             if lo < hi:
                 assert L.upload_bytes(lo, hi) > 0
+
+
+def test_fastdiv_formula():
+    """The kernels divide by a region's column count with a multiply and a shift
+    (Granlund-Montgomery): floor(n / d) == (n * m) >> (32 + l - 1) with
+    l = ceil(log2 d), m = ceil(2^(31+l) / d), for 0 <= n < 2^31.  Checked here
+    for the host-side constants on edge and random cases."""
+    rng = np.random.default_rng(3)
+    ds = [2, 3, 5, 7, 8, 24, 360, 720, 2880, 4096, 5760, 14336, 28672, (1 << 23) - 1, 1 << 23]
+    ds += [int(x) for x in rng.integers(2, 1 << 24, 200)]
+    for d in ds:
+        l = (d - 1).bit_length()
+        m = ((1 << (31 + l)) + d - 1) // d
+        assert m < (1 << 32)
+        ns = [0, 1, d - 1, d, d + 1, (1 << 31) - 1, (1 << 31) - d] + [int(x) for x in rng.integers(0, 1 << 31, 2000)]
+        for n in ns:
+            assert ((n * m) >> 32) >> (l - 1) == n // d, (n, d)

@@ -129,3 +129,17 @@ def test_int8_rint_is_half_even():
     q, s = C.quant_int8_absmax(x)
     assert s == 1.0
     assert list(q) == [127, 0, 2, 2, 0, -2, -2]
+
+
+def test_tiny_blocks_take_the_division_or_zero_path():
+    # reciprocal overflows: codes come from x / s and still span the range
+    x = np.array([3e-38, -1.5e-38, 1e-39, 0.0], np.float32)
+    s, r, mode = C.block_scale(np.max(np.abs(x)), 127)
+    assert mode == 2 and not np.isfinite(r) and s > 0
+    q, s2 = C.quant_int8_absmax(x)
+    assert s2 == s and q[0] == 127 and abs(int(q[1]) + 64) <= 1 and q[3] == 0  # s is subnormal here
+    # scale underflows to zero: zero codes, zero scale
+    q, s3 = C.quant_uint8_absmax(np.array([1e-45, 0.0], np.float32))
+    assert s3 == 0 and not q.any()
+    # ordinary block: reciprocal path
+    assert C.block_scale(np.float32(2.0), 127)[2] == 1

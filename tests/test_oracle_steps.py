@@ -84,7 +84,7 @@ HP = dict(lr=1e-3, b1=0.9, b2=0.999, eps=1e-8)
 
 def test_adam_hparams():
     hp = A.adam_hparams(t=10, **HP)
-    assert hp["bc1"] == np.float32(1 - 0.9 ** 10) and hp["omb2"] == np.float32(0.001)
+    assert hp["rbc1"] == np.float32(1 / (1 - 0.9 ** 10)) and hp["omb2"] == np.float32(0.001)
     assert all(v.dtype == np.float32 for v in hp.values())
 
 
