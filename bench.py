@@ -399,8 +399,10 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def muon_launches(muon):
-    return muon.bq.muon_launch_count(muon.mats) if hasattr(muon.bq, "muon_launch_count") else 0
+def muon_launches(muon, steps=5):
+    """Kernels one bq_muon_ns call launches: per matrix a norm reduction, a
+    scaled (transposing) copy, three GEMMs per step and the copy out."""
+    return len(muon.mats) * (3 + 3 * steps)
 
 
 def run_reference(args):

@@ -215,4 +215,8 @@ int bq_muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float
   return muon_ns(batch, mats, steps, a, b, c, eps, ws, ws_bytes, stream);
 }
 
+int bq_muon_ns_check(const void* ws, size_t ws_bytes, bq_stream_t stream) {
+  return muon_ns_check(ws, ws_bytes, stream);
+}
+
 }  // extern "C"

@@ -140,6 +140,7 @@ int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, floa
 int muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes);
 int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws,
             size_t ws_bytes, void* stream);
+int muon_ns_check(const void* ws, size_t ws_bytes, void* stream);
 
 // errors
 int set_error(int code, const std::string& msg);

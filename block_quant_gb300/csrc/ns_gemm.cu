@@ -1,17 +1,542 @@
-// Muon Newton-Schulz on tcgen05 tensor cores (placeholder until the GEMM lands).
+// Muon's Newton-Schulz orthogonalisation on GB300 tensor cores (sm_103a).
+//
+// Muon needs the whole 2-D matrix at one root rank, which runs the Newton-Schulz
+// iteration (feynmanwiki walkthrough of veScale-FSDP, paper section 6.3).  Per
+// matrix (a tall one is iterated as its transpose):
+//   X = x / (||x||_F + eps);  repeat: A = X X^T;  B = b A + c A A;  X = a X + B X
+// Every product runs in k_gemm: bf16 operands staged by TMA into 128-byte
+// swizzled shared memory, tcgen05.mma issued by one thread into a TMEM fp32
+// accumulator, an epilogue reading TMEM with tcgen05.ld and writing
+// D = alpha*acc + beta*C in bf16.  A is symmetric, so A A is computed as A A^T
+// (both operands K-major); B X takes X as an MN-major operand.
+//
+// Every wait on an mbarrier is bounded: on timeout the kernel records an error
+// word in the workspace, drains its own copies, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
 
 #include "bq_internal.h"
 
 namespace bq {
+namespace {
 
-int muon_ns_workspace(int, const bq_mat*, size_t* bytes) {
-  if (bytes) *bytes = 0;
-  return set_error(BQ_EDEVICE, "bq_muon_ns: not built");
+// ---------------------------------------------------------------- tile geometry
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int TMEM_COLS = 256;     // one 128 x 256 fp32 accumulator
+constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-int muon_ns(int, const bq_mat*, int, float, float, float, float, void*, size_t, void*) {
-  return set_error(BQ_EDEVICE, "bq_muon_ns: not built");
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// bounded wait: false (and an error word) when the phase does not complete
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, int code) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 255) == 255 && clock64() - t0 > kWaitCycles) {
+      if (status) atomicExch(status, code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit accumulator: thread t gets its lane's columns
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- UMMA descriptors
+// Shared-memory matrix descriptor (tcgen05): start address >> 4 in bits 0-13,
+// leading-dimension byte offset >> 4 in bits 16-29, stride-dimension byte
+// offset >> 4 in bits 32-45, the fixed version value 1 in bits 46-47, base
+// offset 0, swizzle mode in bits 61-63 (2 = 128-byte swizzle).
+//  K-major, 128B swizzle: rows of 64 bf16 (128 B), 8-row groups 1024 B apart
+//    (SBO = 1024; LBO unused for this layout).  The k-th 16-element slice of a
+//    row starts 32*k bytes further.
+//  MN-major, 128B swizzle: each k row holds 64 MN-contiguous elements (128 B);
+//    8 k rows form a 1024 B group (SBO = 1024 between groups); 64-element MN
+//    chunks sit LBO apart (one TMA box of BK rows each, LBO = BK * 128 B).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits
+// 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B major in bit 16, N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn_major) << 16) | (uint32_t(n >> 3) << 17) |
+         (uint32_t(m >> 4) << 24);
+}
+
+struct GemmArgs {
+  int M, N, K;
+  float alpha, beta;
+  const __nv_bfloat16* C;  // beta term (may be null when beta == 0), row pitch ldc
+  __nv_bfloat16* D;        // output, row pitch ldd
+  int64_t ldc, ldd;
+  int* status;
+};
+
+// D[M x N] = alpha * (A[M x K] . op(B)) + beta * C.  A: K-major tensor map
+// (box 64 x 128).  B_MN = false: B given as [N x K] K-major (box 64 x 256), the
+// product is A B^T.  B_MN = true: B given as [K x N] N-contiguous (box 64 x 64,
+// four boxes per stage), the product is A B.
+template <bool B_MN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1024-byte-aligned stages
+  unsigned char* gbase = smem_raw + (base - raw);
+  const uint32_t bar_base = base + STAGES * STAGE_BYTES;
+  auto full_bar = [&](int s) { return bar_base + 8u * uint32_t(s); };
+  auto empty_bar = [&](int s) { return bar_base + 8u * uint32_t(STAGES + s); };
+  const uint32_t acc_bar = bar_base + 8u * uint32_t(2 * STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 1));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nk = (g.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    int issued = 0;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = uint32_t(kb / STAGES) & 1u;
+      if (!mbar_wait(empty_bar(s), ph ^ 1u, g.status, 1)) break;
+      const uint32_t a_dst = base + uint32_t(s) * STAGE_BYTES;
+      const uint32_t b_dst = a_dst + A_STAGE;
+      mbar_expect_tx(full_bar(s), STAGE_BYTES);
+      tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
+      if (B_MN) {
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + uint32_t(j) * (BK * 128), &tmB, n0 + 64 * j, kb * BK, full_bar(s));
+      } else {
+        tma_load_2d(b_dst, &tmB, kb * BK, n0, full_bar(s));
+      }
+      issued = kb + 1;
+    }
+    // drain: the last load issued to each stage has landed before this CTA can exit
+    for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
+      mbar_wait(full_bar(kb % STAGES), uint32_t(kb / STAGES) & 1u, g.status, 2);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, B_MN ? 1 : 0);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      if (!mbar_wait(full_bar(s), uint32_t(kb / STAGES) & 1u, g.status, 3)) break;
+      tc_fence_after();
+      const uint32_t a_addr = base + uint32_t(s) * STAGE_BYTES;
+      const uint32_t b_addr = a_addr + A_STAGE;
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint64_t ad = sdesc(a_addr + 32u * kk, 16, 1024);
+        const uint64_t bd = B_MN ? sdesc(b_addr + uint32_t(kk) * 16u * 128u, BK * 128, 1024)
+                                 : sdesc(b_addr + 32u * kk, 16, 1024);
+        mma_bf16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+      }
+      mma_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+    }
+    mma_commit(acc_bar);  // accumulator complete (also after an early exit)
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> registers -> alpha*acc + beta*C -> bf16
+    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    const int row = m0 + 32 * q + lane;
+    const bool ok = mbar_wait(acc_bar, 0, g.status, 4);
+    tc_fence_after();
+    if (ok) {
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(32 * c), r);
+        const int col0 = n0 + 32 * c;
+        if (row >= g.M || col0 >= g.N) continue;
+        __nv_bfloat16* drow = g.D + int64_t(row) * g.ldd;
+        const __nv_bfloat16* crow = g.C ? g.C + int64_t(row) * g.ldc : nullptr;
+        const bool vec = col0 + 32 <= g.N && ((reinterpret_cast<uintptr_t>(drow + col0) | (crow ? reinterpret_cast<uintptr_t>(crow + col0) : 0)) & 15) == 0;
+        if (vec) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float cv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (crow && g.beta != 0.f) {
+              const uint4 cw = *reinterpret_cast<const uint4*>(crow + col0 + 8 * v);
+              const __nv_bfloat162* cp = reinterpret_cast<const __nv_bfloat162*>(&cw);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 f = __bfloat1622float2(cp[j]);
+                cv[2 * j] = f.x;
+                cv[2 * j + 1] = f.y;
+              }
+            }
+            uint4 ow;
+            __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ow);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = g.alpha * __uint_as_float(r[8 * v + 2 * j]) + g.beta * cv[2 * j];
+              const float hi = g.alpha * __uint_as_float(r[8 * v + 2 * j + 1]) + g.beta * cv[2 * j + 1];
+              op[j] = __floats2bfloat162_rn(lo, hi);
+            }
+            *reinterpret_cast<uint4*>(drow + col0 + 8 * v) = ow;
+          }
+        } else {
+          for (int j = 0; j < 32 && col0 + j < g.N; ++j) {
+            const float cv = (crow && g.beta != 0.f) ? __bfloat162float(crow[col0 + j]) : 0.f;
+            drow[col0 + j] = __float2bfloat16_rn(g.alpha * __uint_as_float(r[j]) + g.beta * cv);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- normalisation and copies
+
+constexpr int kRedThreads = 256, kRedBlocks = 1024;
+
+// partial sums of x^2 (fp32) per block, x: rows x cols bf16 with pitch ld
+__global__ void __launch_bounds__(kRedThreads) k_sumsq(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols,
+                                                      int64_t ld, float* __restrict__ partial) {
+  float acc = 0.f;
+  const int64_t n = rows * cols;
+  for (int64_t i = int64_t(blockIdx.x) * kRedThreads + threadIdx.x; i < n; i += int64_t(gridDim.x) * kRedThreads) {
+    const int64_t r = i / cols, c = i - r * cols;
+    const float v = __bfloat162float(x[r * ld + c]);
+    acc = fmaf(v, v, acc);
+  }
+  __shared__ float red[kRedThreads / 32];
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kRedThreads / 32; ++w) t += red[w];
+    partial[blockIdx.x] = t;
+  }
+}
+
+__device__ __forceinline__ float inv_norm(const float* __restrict__ partial, int nparts, float eps) {
+  // every block sums the partials in the same order: one deterministic norm
+  __shared__ float s_inv;
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < nparts; ++i) t += double(partial[i]);
+    s_inv = 1.f / (sqrtf(float(t)) + eps);
+  }
+  __syncthreads();
+  return s_inv;
+}
+
+// X0 = x * inv_norm (transposed when `transpose`), X0 row pitch ldo.  32 x 32
+// tiles through shared memory so both sides stay coalesced.
+__global__ void __launch_bounds__(256) k_scale_copy(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols,
+                                                   int64_t ldx, __nv_bfloat16* __restrict__ out, int64_t ldo,
+                                                   int transpose, const float* __restrict__ partial, int nparts,
+                                                   float eps) {
+  const float s = partial ? inv_norm(partial, nparts, eps) : 1.f;
+  __shared__ float tile[32][33];
+  const int64_t r0 = int64_t(blockIdx.y) * 32, c0 = int64_t(blockIdx.x) * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t r = r0 + i, c = c0 + tx;
+    tile[i][tx] = (r < rows && c < cols) ? __bfloat162float(x[r * ldx + c]) * s : 0.f;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    if (transpose) {
+      const int64_t orow = c0 + i, ocol = r0 + tx;  // out is cols x rows
+      if (orow < cols && ocol < rows) out[orow * ldo + ocol] = __float2bfloat16_rn(tile[tx][i]);
+    } else {
+      const int64_t r = r0 + i, c = c0 + tx;
+      if (r < rows && c < cols) out[r * ldo + c] = __float2bfloat16_rn(tile[i][tx]);
+    }
+  }
+}
+
+int check(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  return BQ_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps (driver entry point at run time)
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map: inner extent `inner` (contiguous), outer extent `outer`,
+// row pitch `ld` elements, box inner 64 (128 bytes, the swizzle span) x box_outer
+int make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
+  EncodeTiled enc = encoder();
+  if (!enc) return set_error(BQ_EDEVICE, "bq_muon_ns: cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+  const cuuint32_t box[2] = {64u, cuuint32_t(box_outer)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(BQ_EINVAL, "bq_muon_ns: tensor map encoding failed (" + std::to_string(int(r)) + ")");
+  return BQ_OK;
+}
+
+int64_t pitch_of(int64_t cols) { return (cols + 63) / 64 * 64; }  // 128-byte rows
+
+struct NsPlan {
+  int64_t m, n;        // iterated shape (m <= n)
+  bool tall;
+  int64_t ldx, lda;    // pitches of X (m x n) and A, B (m x m)
+  size_t off_part, off_status, off_x0, off_x1, off_a, off_b, bytes;
+};
+
+NsPlan ns_plan(const bq_mat& t) {
+  NsPlan p;
+  p.tall = t.rows > t.cols;
+  p.m = p.tall ? t.cols : t.rows;
+  p.n = p.tall ? t.rows : t.cols;
+  p.ldx = pitch_of(p.n);
+  p.lda = pitch_of(p.m);
+  size_t o = 0;
+  p.off_part = o;
+  o += kRedBlocks * sizeof(float);
+  p.off_status = o;
+  o += 256;
+  p.off_x0 = o;
+  o += size_t(p.m) * p.ldx * 2;
+  o = (o + 1023) / 1024 * 1024;
+  p.off_x1 = o;
+  o += size_t(p.m) * p.ldx * 2;
+  o = (o + 1023) / 1024 * 1024;
+  p.off_a = o;
+  o += size_t(p.m) * p.lda * 2;
+  o = (o + 1023) / 1024 * 1024;
+  p.off_b = o;
+  o += size_t(p.m) * p.lda * 2;
+  p.bytes = (o + 1023) / 1024 * 1024;
+  return p;
+}
+
+int check_mat(const bq_mat& t) {
+  if (!t.x || !t.y || t.rows < 1 || t.cols < 1 || t.ld_x < t.cols || t.ld_y < t.cols)
+    return set_error(BQ_EINVAL, "bq_muon_ns: bad matrix descriptor");
+  if (t.rows > (int64_t(1) << 20) || t.cols > (int64_t(1) << 20) || t.rows * t.cols > (int64_t(1) << 31))
+    return set_error(BQ_EINVAL, "bq_muon_ns: matrix too large");
+  if ((reinterpret_cast<uintptr_t>(t.x) | reinterpret_cast<uintptr_t>(t.y)) & 1)
+    return set_error(BQ_EALIGN, "bq_muon_ns: matrices must be 2-byte aligned");
+  return BQ_OK;
+}
+
+int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, cudaStream_t s) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(k_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    cudaFuncSetAttribute(k_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+  });
+  const dim3 grid(unsigned((g.N + BN - 1) / BN), unsigned((g.M + BM - 1) / BM));
+  if (b_mn)
+    k_gemm<true><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, g);
+  else
+    k_gemm<false><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, g);
+  return check("bq_muon_ns (gemm)");
+}
+
+}  // namespace
+
+int muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes) {
+  if (!bytes || batch < 0 || (batch > 0 && !mats)) return set_error(BQ_EINVAL, "bq_muon_ns_workspace: bad arguments");
+  size_t need = 256;
+  for (int i = 0; i < batch; ++i) {
+    if (int rc = check_mat(mats[i])) return rc;
+    need = std::max(need, ns_plan(mats[i]).bytes);
+  }
+  *bytes = need;
+  return BQ_OK;
+}
+
+int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws, size_t ws_bytes,
+            void* stream) {
+  if (batch < 0 || (batch > 0 && !mats) || steps < 0) return set_error(BQ_EINVAL, "bq_muon_ns: bad arguments");
+  if (batch > 0 && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)))
+    return set_error(BQ_EALIGN, "bq_muon_ns: workspace must be 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < batch; ++i) {
+    const bq_mat& t = mats[i];
+    if (int rc = check_mat(t)) return rc;
+    const NsPlan p = ns_plan(t);
+    if (ws_bytes < p.bytes) return set_error(BQ_ENOSPC, "bq_muon_ns: workspace too small");
+    auto* w = static_cast<unsigned char*>(ws);
+    float* part = reinterpret_cast<float*>(w + p.off_part);
+    int* status = reinterpret_cast<int*>(w + p.off_status);
+    auto* X0 = reinterpret_cast<__nv_bfloat16*>(w + p.off_x0);
+    auto* X1 = reinterpret_cast<__nv_bfloat16*>(w + p.off_x1);
+    auto* A = reinterpret_cast<__nv_bfloat16*>(w + p.off_a);
+    auto* B = reinterpret_cast<__nv_bfloat16*>(w + p.off_b);
+    const auto* x = static_cast<const __nv_bfloat16*>(t.x);
+    auto* y = static_cast<__nv_bfloat16*>(t.y);
+
+    // the device error word starts clear for every matrix
+    if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return check("bq_muon_ns (status)");
+    // normalise into X0 (transposed for a tall input)
+    k_sumsq<<<kRedBlocks, kRedThreads, 0, s>>>(x, t.rows, t.cols, t.ld_x, part);
+    if (int rc = check("bq_muon_ns (norm)")) return rc;
+    const dim3 cg(unsigned((t.cols + 31) / 32), unsigned((t.rows + 31) / 32));
+    k_scale_copy<<<cg, 256, 0, s>>>(x, t.rows, t.cols, t.ld_x, X0, p.ldx, p.tall ? 1 : 0, part, kRedBlocks, eps);
+    if (int rc = check("bq_muon_ns (scale)")) return rc;
+
+    // tensor maps: X as K-major A operand / K-major B operand / MN-major B operand, A, B
+    CUtensorMap mXa[2], mXb[2], mXmn[2], mAa, mAb, mBa;
+    __nv_bfloat16* Xs[2] = {X0, X1};
+    for (int j = 0; j < 2; ++j) {
+      if (int rc = make_map(&mXa[j], Xs[j], p.n, p.m, p.ldx, BM)) return rc;
+      if (int rc = make_map(&mXb[j], Xs[j], p.n, p.m, p.ldx, BN)) return rc;
+      if (int rc = make_map(&mXmn[j], Xs[j], p.n, p.m, p.ldx, BK)) return rc;
+    }
+    if (int rc = make_map(&mAa, A, p.m, p.m, p.lda, BM)) return rc;
+    if (int rc = make_map(&mAb, A, p.m, p.m, p.lda, BN)) return rc;
+    if (int rc = make_map(&mBa, B, p.m, p.m, p.lda, BM)) return rc;
+
+    int cur = 0;
+    for (int it = 0; it < steps; ++it) {
+      const int nxt = cur ^ 1;
+      // A = X X^T
+      GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status};
+      if (int rc = gemm(false, mXa[cur], mXb[cur], g1, s)) return rc;
+      // B = c (A A^T) + b A   (A symmetric)
+      GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status};
+      if (int rc = gemm(false, mAa, mAb, g2, s)) return rc;
+      // X' = B X + a X
+      GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status};
+      if (int rc = gemm(true, mBa, mXmn[cur], g3, s)) return rc;
+      cur = nxt;
+    }
+    // y = X (transposed back for a tall input)
+    const dim3 og(unsigned((p.n + 31) / 32), unsigned((p.m + 31) / 32));
+    k_scale_copy<<<og, 256, 0, s>>>(Xs[cur], p.m, p.n, p.ldx, y, t.ld_y, p.tall ? 1 : 0, nullptr, 0, 0.f);
+    if (int rc = check("bq_muon_ns (copy out)")) return rc;
+  }
+  return BQ_OK;
+}
+
+int muon_ns_check(const void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kRedBlocks * sizeof(float) + sizeof(int)) return set_error(BQ_EINVAL, "bq_muon_ns_check: bad workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int status = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(&status, static_cast<const unsigned char*>(ws) + kRedBlocks * sizeof(float), sizeof(int),
+                   cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string("bq_muon_ns_check: ") + cudaGetErrorString(e));
+  if (status) return set_error(BQ_ECUDA, "bq_muon_ns: a device wait timed out (site " + std::to_string(status) + ")");
+  return BQ_OK;
 }
 
 }  // namespace bq

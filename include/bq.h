@@ -193,11 +193,21 @@ int bq_quant_fp8(const bq_shard* shard, const float* master, uint8_t* fp8_out, f
  *   X = x / (||x||_F + eps); repeat steps: A = X X^T; B = b A + c A A; X = a X + B X
  * on tcgen05 tensor cores: bf16 operands, fp32 accumulation, bf16 storage of
  * X, A, B between products, fp32 Frobenius norm.
- * mats: host array; ws: device workspace of ws_bytes (bf16 scratch for X, A, B
- * and a few fp32 words), size from bq_muon_ns_workspace. */
+ * mats: host array; ws: device workspace of ws_bytes, 256-byte aligned (bf16
+ * scratch for X, A, B, fp32 partial norms and an error word), size from
+ * bq_muon_ns_workspace; matrices are processed one after another and reuse it.
+ * Errors: BQ_EINVAL (bad descriptor, rows or cols above 2^20), BQ_EALIGN,
+ * BQ_ENOSPC, BQ_EDEVICE (driver entry point for tensor maps unavailable). */
 int bq_muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes);
 int bq_muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws,
                size_t ws_bytes, bq_stream_t stream);
+
+/* bq_muon_ns_check - synchronise `stream` and read the workspace's device error
+ * word: every wait inside the tensor-core kernels gives up after about two
+ * seconds, records where, and lets the kernel exit cleanly.  BQ_OK if no wait
+ * timed out during the last bq_muon_ns on this workspace, BQ_ECUDA otherwise
+ * (or on a CUDA error). */
+int bq_muon_ns_check(const void* ws, size_t ws_bytes, bq_stream_t stream);
 
 #ifdef __cplusplus
 }
