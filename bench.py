@@ -217,7 +217,7 @@ class MuonBatch:
 
         import block_quant_gb300 as bq
 
-        self.bq = bq
+        self.bq, self.torch = bq, torch
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
         self.xs = [(torch.randn(r, c, generator=g, device=dev) * 1e-3).to(torch.bfloat16) for r, c in shapes]
@@ -229,6 +229,20 @@ class MuonBatch:
 
     def run(self, stream):
         self.bq.muon_ns(self.mats, self.ws, stream=stream)
+
+    def pin_host(self):
+        torch = self.torch
+        self.hx = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in self.xs]
+        self.hy = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in self.ys]
+        self.h2d = sum(x.numel() * 2 for x in self.xs)
+        self.d2h = sum(y.numel() * 2 for y in self.ys)
+
+    def e2e(self, stream):
+        for x, hx in zip(self.xs, self.hx):
+            x.copy_(hx, non_blocking=True)
+        self.run(stream)
+        for y, hy in zip(self.ys, self.hy):
+            hy.copy_(y, non_blocking=True)
 
 
 def cpu_baseline(seconds=12.0):
@@ -327,28 +341,42 @@ def run_ours(args):
     dbuf_ms = statistics.mean(p + a for p, a in zip(pack_ms, adam_ms))
 
     # end to end through the public API: H2D of the step's gradients from pinned
-    # host memory, the step, D2H of the FP8 staging buffer and its scales
+    # host memory, pack + Adam + FP8, D2H of the FP8 staging buffer and scales
     step.pin_host()
-    for _ in range(2):
+
+    def e2e_step():
         for i, g in step.grads.items():
             g.copy_(step.host_grads[i], non_blocking=True)
-        one_step()
+        step.pack(stream)
+        step.adam(stream)
         step.host_fp8.copy_(step.fp8, non_blocking=True)
         step.host_fs.copy_(step.fs, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    ke = max(10, args.steps // 4)
+    ke = max(10, args.steps // 2)
     e0.record(stream)
     for _ in range(ke):
-        for i, g in step.grads.items():
-            g.copy_(step.host_grads[i], non_blocking=True)
-        one_step()
-        step.host_fp8.copy_(step.fp8, non_blocking=True)
-        step.host_fs.copy_(step.fs, non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / ke
+    muon_e2e = None
+    if muon:
+        muon.pin_host()
+        for _ in range(2):
+            muon.e2e(stream)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        km = 5
+        for _ in range(km):
+            muon.e2e(stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        muon_e2e = e0.elapsed_time(e1) / km
 
     local_vals = torch.tensor([total_ms / args.steps, dbuf_ms, statistics.mean(muon_ms), e2e_ms],
                               dtype=torch.float64, device=dev)
@@ -391,7 +419,10 @@ def run_ours(args):
             tf = world * muon.flops / (muon_ms_max * 1e-3) / 1e12
             line["muon"] = {"value": round(tf, 1), "unit": "TFLOP/s", "ms": round(muon_ms_max, 3),
                             "flops": muon.flops, "frac": round(tf / world / pk["bf16_sus"], 4),
-                            "peak": pk["bf16_sus"], "peak_source": f"{pk['src']} bf16_tflops_sustained"}
+                            "peak": pk["bf16_sus"], "peak_source": f"{pk['src']} bf16_tflops_sustained",
+                            "e2e": {"value": round(muon.flops / (muon_e2e * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                                    "h2d_bytes_per_step": muon.h2d, "d2h_bytes_per_step": muon.d2h,
+                                    "ms_per_step": round(muon_e2e, 3)}}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
@@ -400,9 +431,10 @@ def run_ours(args):
 
 
 def muon_launches(muon, steps=5):
-    """Kernels one bq_muon_ns call launches: per matrix a norm reduction, a
-    scaled (transposing) copy, three GEMMs per step and the copy out."""
-    return len(muon.mats) * (3 + 3 * steps)
+    """Kernels one bq_muon_ns call launches: per matrix a sum-of-squares
+    reduction, its one-block finish, a scaled (transposing) copy, three GEMMs
+    per step and the copy out."""
+    return len(muon.mats) * (4 + 3 * steps)
 
 
 def run_reference(args):

@@ -289,15 +289,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
 constexpr int kRedThreads = 256, kRedBlocks = 1024;
 
-// partial sums of x^2 (fp32) per block, x: rows x cols bf16 with pitch ld
+// partial sums of x^2 (fp32) per block, x: rows x cols bf16 with pitch ld;
+// blocks stride over rows, threads over columns
 __global__ void __launch_bounds__(kRedThreads) k_sumsq(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols,
                                                       int64_t ld, float* __restrict__ partial) {
   float acc = 0.f;
-  const int64_t n = rows * cols;
-  for (int64_t i = int64_t(blockIdx.x) * kRedThreads + threadIdx.x; i < n; i += int64_t(gridDim.x) * kRedThreads) {
-    const int64_t r = i / cols, c = i - r * cols;
-    const float v = __bfloat162float(x[r * ld + c]);
-    acc = fmaf(v, v, acc);
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const __nv_bfloat16* row = x + r * ld;
+    for (int64_t c = threadIdx.x; c < cols; c += kRedThreads) {
+      const float v = __bfloat162float(row[c]);
+      acc = fmaf(v, v, acc);
+    }
   }
   __shared__ float red[kRedThreads / 32];
   for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
@@ -310,25 +312,29 @@ __global__ void __launch_bounds__(kRedThreads) k_sumsq(const __nv_bfloat16* __re
   }
 }
 
-__device__ __forceinline__ float inv_norm(const float* __restrict__ partial, int nparts, float eps) {
-  // every block sums the partials in the same order: one deterministic norm
-  __shared__ float s_inv;
-  if (threadIdx.x == 0) {
-    double t = 0.0;
-    for (int i = 0; i < nparts; ++i) t += double(partial[i]);
-    s_inv = 1.f / (sqrtf(float(t)) + eps);
-  }
+// 1 / (||x||_F + eps) from the partial sums (one block, fixed summation order)
+__global__ void __launch_bounds__(kRedThreads) k_inv_norm(const float* __restrict__ partial, int nparts, float eps,
+                                                         float* __restrict__ inv) {
+  double t = 0.0;
+  for (int i = threadIdx.x; i < nparts; i += kRedThreads) t += double(partial[i]);
+  __shared__ double red[kRedThreads / 32];
+  for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = t;
   __syncthreads();
-  return s_inv;
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < kRedThreads / 32; ++w) tot += red[w];
+    *inv = 1.f / (sqrtf(float(tot)) + eps);
+  }
 }
 
-// X0 = x * inv_norm (transposed when `transpose`), X0 row pitch ldo.  32 x 32
+// out = x * (*inv) (transposed when `transpose`; inv NULL: plain copy), out row
+// pitch ldo.  32 x 32
 // tiles through shared memory so both sides stay coalesced.
 __global__ void __launch_bounds__(256) k_scale_copy(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols,
                                                    int64_t ldx, __nv_bfloat16* __restrict__ out, int64_t ldo,
-                                                   int transpose, const float* __restrict__ partial, int nparts,
-                                                   float eps) {
-  const float s = partial ? inv_norm(partial, nparts, eps) : 1.f;
+                                                   int transpose, const float* __restrict__ inv) {
+  const float s = inv ? *inv : 1.f;
   __shared__ float tile[32][33];
   const int64_t r0 = int64_t(blockIdx.y) * 32, c0 = int64_t(blockIdx.x) * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
@@ -476,6 +482,7 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
     auto* w = static_cast<unsigned char*>(ws);
     float* part = reinterpret_cast<float*>(w + p.off_part);
     int* status = reinterpret_cast<int*>(w + p.off_status);
+    float* inv = reinterpret_cast<float*>(w + p.off_status + 16);  // 1 / (||x||_F + eps)
     auto* X0 = reinterpret_cast<__nv_bfloat16*>(w + p.off_x0);
     auto* X1 = reinterpret_cast<__nv_bfloat16*>(w + p.off_x1);
     auto* A = reinterpret_cast<__nv_bfloat16*>(w + p.off_a);
@@ -489,7 +496,9 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
     k_sumsq<<<kRedBlocks, kRedThreads, 0, s>>>(x, t.rows, t.cols, t.ld_x, part);
     if (int rc = check("bq_muon_ns (norm)")) return rc;
     const dim3 cg(unsigned((t.cols + 31) / 32), unsigned((t.rows + 31) / 32));
-    k_scale_copy<<<cg, 256, 0, s>>>(x, t.rows, t.cols, t.ld_x, X0, p.ldx, p.tall ? 1 : 0, part, kRedBlocks, eps);
+    k_inv_norm<<<1, kRedThreads, 0, s>>>(part, kRedBlocks, eps, inv);
+    if (int rc = check("bq_muon_ns (inv norm)")) return rc;
+    k_scale_copy<<<cg, 256, 0, s>>>(x, t.rows, t.cols, t.ld_x, X0, p.ldx, p.tall ? 1 : 0, inv);
     if (int rc = check("bq_muon_ns (scale)")) return rc;
 
     // tensor maps: X as K-major A operand / K-major B operand / MN-major B operand, A, B
@@ -520,7 +529,7 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
     }
     // y = X (transposed back for a tall input)
     const dim3 og(unsigned((p.n + 31) / 32), unsigned((p.m + 31) / 32));
-    k_scale_copy<<<og, 256, 0, s>>>(Xs[cur], p.m, p.n, p.ldx, y, t.ld_y, p.tall ? 1 : 0, nullptr, 0, 0.f);
+    k_scale_copy<<<og, 256, 0, s>>>(Xs[cur], p.m, p.n, p.ldx, y, t.ld_y, p.tall ? 1 : 0, nullptr);
     if (int rc = check("bq_muon_ns (copy out)")) return rc;
   }
   return BQ_OK;
