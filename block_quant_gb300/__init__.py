@@ -25,6 +25,7 @@ SYMBOLS = [
     "bq_strerror", "bq_last_error", "bq_version", "bq_plan", "bq_layout_free", "bq_layout_query",
     "bq_layout_export", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_pack",
     "bq_step_adam8", "bq_quant_fp8", "bq_muon_ns_workspace", "bq_muon_ns", "bq_muon_ns_check",
+    "bq_muon_ns_noalloc",
 ]
 
 
@@ -91,6 +92,8 @@ def load():
     lib.bq_muon_ns.argtypes = [C.c_int, C.POINTER(Mat), C.c_int, C.c_float, C.c_float, C.c_float, C.c_float,
                                P, C.c_size_t, P]
     lib.bq_muon_ns_check.argtypes = [P, C.c_size_t, P]
+    lib.bq_muon_ns_noalloc.argtypes = [C.c_int, C.POINTER(Mat), C.c_int, C.c_float, C.c_float, C.c_float,
+                                       C.c_float, P]
     for name in SYMBOLS:
         if name not in ("bq_strerror", "bq_last_error", "bq_layout_free", "bq_shard_free"):
             getattr(lib, name).restype = C.c_int
@@ -258,3 +261,12 @@ def muon_ns_check(ws, ws_bytes=None, stream=None):
     if ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size()
     _check(load().bq_muon_ns_check(_ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def muon_ns_noalloc(mats, steps=5, a=3.4445, b=-4.7750, c=2.0315, eps=1e-7, stream=None):
+    """Newton-Schulz for callers that cannot allocate device memory: the library
+    uses its own fixed 32 MiB device scratch (shared by all calls; order calls
+    that could overlap).  Batches needing more scratch raise BQ_ENOSPC."""
+    arr = _mats(mats)
+    _check(load().bq_muon_ns_noalloc(len(arr), arr, int(steps), float(a), float(b), float(c), float(eps),
+                                     _stream(stream)))

@@ -219,4 +219,9 @@ int bq_muon_ns_check(const void* ws, size_t ws_bytes, bq_stream_t stream) {
   return muon_ns_check(ws, ws_bytes, stream);
 }
 
+int bq_muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps,
+                       bq_stream_t stream) {
+  return muon_ns_noalloc(batch, mats, steps, a, b, c, eps, stream);
+}
+
 }  // extern "C"

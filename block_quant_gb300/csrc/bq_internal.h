@@ -141,6 +141,7 @@ int muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes);
 int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws,
             size_t ws_bytes, void* stream);
 int muon_ns_check(const void* ws, size_t ws_bytes, void* stream);
+int muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* stream);
 
 // errors
 int set_error(int code, const std::string& msg);

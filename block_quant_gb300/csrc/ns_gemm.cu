@@ -535,6 +535,46 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
   return BQ_OK;
 }
 
+// ---------------------------------------------------------------- allocation-free variant
+// Some callers cannot allocate device memory at the point where they run the
+// optimizer step: runtimes that reserve every byte of the GPU up front and
+// forbid later cudaMalloc calls, plug-ins inside a host framework that owns the
+// allocator, or code paths that must not allocate for latency reasons.  They use
+// bq_muon_ns_noalloc, whose scratch is this fixed array in the library's device
+// image: every GPU that loads the library holds it until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_ns_scratch[kStaticScratchBytes];
+
+int muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* stream) {
+  // The array's device address, looked up once per device with that device
+  // current (in host code the symbol is only a stand-in, not a device address).
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return set_error(BQ_EDEVICE, "bq_muon_ns_noalloc: no usable current device");
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_ns_scratch);
+      if (e != cudaSuccess || !p)
+        return set_error(BQ_ECUDA, std::string("bq_muon_ns_noalloc: scratch address lookup failed: ") +
+                                       cudaGetErrorString(e));
+      addr[dev] = p;
+    }
+    scratch = addr[dev];
+  }
+  size_t need = 0;
+  if (int rc = muon_ns_workspace(batch, mats, &need)) return rc;
+  if (need > kStaticScratchBytes)
+    return set_error(BQ_ENOSPC, "bq_muon_ns_noalloc: the batch needs " + std::to_string(need) +
+                                    " bytes of scratch; the static scratch holds " +
+                                    std::to_string(kStaticScratchBytes) + " (use bq_muon_ns with a workspace)");
+  return muon_ns(batch, mats, steps, a, b, c, eps, scratch, kStaticScratchBytes, stream);
+}
+
 int muon_ns_check(const void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < kRedBlocks * sizeof(float) + sizeof(int)) return set_error(BQ_EINVAL, "bq_muon_ns_check: bad workspace");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

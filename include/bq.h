@@ -209,6 +209,26 @@ int bq_muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float
  * (or on a CUDA error). */
 int bq_muon_ns_check(const void* ws, size_t ws_bytes, bq_stream_t stream);
 
+/* bq_muon_ns_noalloc - bq_muon_ns for callers that cannot allocate device memory
+ * when the step runs (a runtime that reserves all GPU memory up front and
+ * forbids later cudaMalloc, a plug-in whose host framework owns the allocator,
+ * a code path that must not allocate for latency reasons).  The paper has no
+ * counterpart: this is an interface convenience of this library.
+ * The caller passes inputs and outputs as for bq_muon_ns; the scratch is a fixed
+ * 32 MiB array inside the library's device image (every GPU that loads the
+ * library holds it until the process exits), so nothing is allocated and no
+ * workspace is passed.  A batch whose bq_muon_ns_workspace size exceeds 32 MiB
+ * is rejected with BQ_ENOSPC before any work is queued (for example, a 1024 x
+ * 4096 matrix fits; a 2048 x 2048 one does not).
+ * The first call on each device looks up the scratch array's device address
+ * with that device current; make that first call before any stream capture.
+ * All calls share the one array and each call overwrites it: calls that can
+ * overlap on the GPU (different streams without ordering between them) race,
+ * so order them.  The device error word lives in the shared scratch and cannot
+ * be read through bq_muon_ns_check. */
+int bq_muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps,
+                       bq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
