@@ -49,6 +49,23 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+def recorded_traffic(call):
+    """DRAM bytes per launch of `call` from the committed ncu record, or None when
+    the kernel source changed since the counters were taken."""
+    import hashlib
+
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(call)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
+        return None
+    return rec["traffic_bytes_per_launch"]
+
+
 # ----------------------------------------------------------------------------- algorithmic bytes
 
 def step_bytes(table, dev_lo, dev_hi):
@@ -97,6 +114,27 @@ def muon_flops(shapes, steps=5):
         m, n = min(r, c), max(r, c)
         tot += steps * (4 * m * m * n + 2 * m ** 3)
     return tot
+
+
+# ----------------------------------------------------------------------------- ranks
+
+
+def max_over_ranks(vals, world, device=None):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest rank
+    sets the job's time)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank, world, ms):
+    """Whole-job rate: every rank processed units_per_rank units (weak scaling)
+    in at most ms milliseconds."""
+    return world * units_per_rank / (ms * 1e-3)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -378,15 +416,12 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         muon_e2e = e0.elapsed_time(e1) / km
 
-    local_vals = torch.tensor([total_ms / args.steps, dbuf_ms, statistics.mean(muon_ms), e2e_ms],
-                              dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(local_vals, op=dist.ReduceOp.MAX)
-    ms_step, dbuf_ms_max, muon_ms_max, e2e_max = local_vals.tolist()
+    ms_step, dbuf_ms_max, muon_ms_max, e2e_max, muon_e2e_max = max_over_ranks(
+        [total_ms / args.steps, dbuf_ms, statistics.mean(muon_ms), e2e_ms, muon_e2e or 0.0], world, device=dev)
     if rank == 0:
         pk = peaks()
         B = step.bytes["total"]
-        value = world * B / (dbuf_ms_max * 1e-3) / 1e9
+        value = job_throughput(B, world, dbuf_ms_max) / 1e9
         adam_mean = statistics.mean(adam_ms)
         adam_gbs = step.bytes["adam"] / (adam_mean * 1e-3) / 1e9
         line = {
@@ -406,23 +441,23 @@ def run_ours(args):
                      "GB/s": round(step.bytes["pack"] / (statistics.mean(pack_ms) * 1e-3) / 1e9, 1)},
             "roofline": {"bound": "hbm", "kernel": "bq_step_adam8 (8-bit Adam + fused FP8)",
                          "achieved": round(adam_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                         "frac": round(adam_gbs / pk["hbm"], 4), "traffic": None,
+                         "frac": round(adam_gbs / pk["hbm"], 4), "traffic": recorded_traffic("bq_step_adam8"),
                          "peak_source": f"{pk['src']} hbm_gbs (STREAM-style copy)",
                          "ms": round(adam_mean, 4), "algorithmic_bytes": step.bytes["adam"]},
-            "e2e": {"value": round(world * B / (e2e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "e2e": {"value": round(job_throughput(B, world, e2e_max) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": step.h2d, "d2h_bytes_per_step": step.d2h,
                     "ms_per_step": round(e2e_max, 4)},
             "gpu_launches": args.steps * (step.launches + (muon_launches(muon) if muon else 0)),
             "clocks": clk,
         }
         if muon:
-            tf = world * muon.flops / (muon_ms_max * 1e-3) / 1e12
+            tf = job_throughput(muon.flops, world, muon_ms_max) / 1e12
             line["muon"] = {"value": round(tf, 1), "unit": "TFLOP/s", "ms": round(muon_ms_max, 3),
                             "flops": muon.flops, "frac": round(tf / world / pk["bf16_sus"], 4),
                             "peak": pk["bf16_sus"], "peak_source": f"{pk['src']} bf16_tflops_sustained",
-                            "e2e": {"value": round(muon.flops / (muon_e2e * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
-                                    "h2d_bytes_per_step": muon.h2d, "d2h_bytes_per_step": muon.d2h,
-                                    "ms_per_step": round(muon_e2e, 3)}}
+                            "e2e": {"value": round(job_throughput(muon.flops, world, muon_e2e_max) / 1e12, 1),
+                                    "unit": "TFLOP/s", "h2d_bytes_per_step": muon.h2d,
+                                    "d2h_bytes_per_step": muon.d2h, "ms_per_step": round(muon_e2e_max, 3)}}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)

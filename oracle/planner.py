@@ -382,5 +382,43 @@ def _blocks(layout, dev_lo, dev_hi, fp8):
                     slot += 1
 
 
+def block_at(layout, dev_lo, dev_hi, pos, fp8=False):
+    """(slot, local positions) of the Adam block (or FP8 tile) holding local
+    position ``pos`` of shards [dev_lo, dev_hi), or None for padding / a tensor
+    without FP8.  Same slot rules as _blocks, for one block."""
+    S = layout.S
+    k = dev_lo + pos // S
+    loff_in = pos - (k - dev_lo) * S
+    first, _, _ = layout.dev_table[k]
+    last, _, _ = layout.dev_table[k + 1]
+    base = layout.dev_table[dev_lo][2 if fp8 else 1]
+    for (kk, i, t_off, ln, loff, mslot, fslot) in layout.intervals[first:last]:
+        if not (loff <= loff_in < loff + ln):
+            continue
+        d = layout.descs[i]
+        if fp8 and not d.fp8:
+            return None
+        slot0 = (fslot if fp8 else mslot) - base
+        pos0 = (k - dev_lo) * S + loff - t_off
+        f = t_off + (loff_in - loff)  # tensor-flat offset
+        if not fp8 and d.adam_kind == ADAM_FLAT256:
+            j = (f - t_off) // 256
+            a = t_off + 256 * j
+            return slot0 + j, pos0 + range_array(a, min(a + 256, t_off + ln))
+        if d.rows == 1:
+            j = (f - t_off) // 128
+            a = t_off + 128 * j
+            return slot0 + j, pos0 + range_array(a, min(a + 128, t_off + ln))
+        C = d.cols
+        r0, r1 = t_off // C, (t_off + ln) // C
+        r, c = f // C, f % C
+        band, ct = (r - r0) // 128, c // 128
+        nct = -(-C // 128)
+        rows = range_array(r0 + 128 * band, min(r0 + 128 * band + 128, r1))
+        cols = range_array(128 * ct, min(128 * ct + 128, C))
+        return slot0 + band * nct + ct, pos0 + (rows[:, None] * C + cols[None, :]).ravel()
+    return None
+
+
 def range_array(a, b):
     return np.arange(a, b, dtype=np.int64)

@@ -119,3 +119,77 @@ def assert_bits_equal(name, got, want):
         gb, wb = got, want
     bad = np.nonzero(gb != wb)[0]
     assert bad.size == 0, f"{name}: {bad.size} of {got.size} differ, first at {bad[:8]}: got {got[bad[:4]]} want {want[bad[:4]]}"
+
+
+def sampled_check(case, got, n_blocks=300, n_tiles=24, seed=0):
+    """Full-size parity on sampled outputs: the whole packed gradient buffer is
+    compared with the oracle's pack; Adam blocks and FP8 tiles holding random
+    tensor elements are recomputed by the oracle one by one; padding of every
+    state buffer must be untouched."""
+    from oracle import adam8 as OA
+    from oracle import fp8 as OF
+    from oracle import pack as OP
+    from oracle import planner as P
+
+    L, lo, hi = case.olayout, case.dev_lo, case.dev_hi
+    sc = np.float32(1.0 / case.V)
+    dbuf = OP.pack(L, lo, hi, case.grads, case.dbuf0, sc, False)
+    assert_bits_equal("dbuf (full)", got["dbuf"], dbuf)
+    covered = np.zeros(case.n, bool)
+    for k, i, t_off, ln, loff, _, _ in L.intervals[L.dev_table[lo][0]:L.dev_table[hi][0]]:
+        covered[(k - lo) * L.S + loff:(k - lo) * L.S + loff + ln] = True
+    assert np.all(got["master"][~covered] == PAD_F32) and np.all(got["m"][~covered] == PAD_I8)
+    assert np.all(got["v"][~covered] == PAD_U8)
+    rng = np.random.default_rng(seed)
+
+    def probes(count):
+        """random tensor positions (padding rejected), with replacement"""
+        out = []
+        while len(out) < count:
+            cand = rng.integers(0, case.n, size=4 * count)
+            out.extend(int(x) for x in cand[covered[cand]])
+        return out[:count]
+
+    p_new = {}
+
+    def run_block(slot, pos):
+        p1, qm, qv, sm, sv = OA.adam8_block(dbuf[pos], case.master[pos], case.m[pos], case.v[pos],
+                                            case.ms[slot], case.vs[slot], case.hp_o)
+        p_new.update(zip(pos.tolist(), p1.tolist()))
+        return p1, qm, qv, sm, sv
+
+    for probe in probes(n_blocks):
+        slot, pos = P.block_at(L, lo, hi, probe)
+        p1, qm, qv, sm, sv = run_block(slot, pos)
+        assert_bits_equal(f"master block {slot}", got["master"][pos], p1)
+        assert_bits_equal(f"m codes block {slot}", got["m"][pos], qm)
+        assert_bits_equal(f"v codes block {slot}", got["v"][pos], qv)
+        assert_bits_equal(f"m scale {slot}", got["ms"][slot:slot + 1], np.array([sm], np.float32))
+        assert_bits_equal(f"v scale {slot}", got["vs"][slot:slot + 1], np.array([sv], np.float32))
+    if got["fp8"] is None:
+        return
+    done = 0
+    for probe in probes(20 * n_tiles):
+        if done >= n_tiles:
+            break
+        hit = P.block_at(L, lo, hi, probe, fp8=True)
+        if hit is None:
+            continue
+        tslot, tpos = hit
+        # every Adam block meeting the tile: blocks are at least 128 elements
+        # long and tile rows are 8-element aligned, so probing every 8th
+        # element finds them all
+        need = set()
+        for e in np.unique(np.concatenate([tpos[::8], tpos[7::8]])):
+            need.add(int(e))
+        for e in sorted(need):
+            if e not in p_new:
+                slot, pos = P.block_at(L, lo, hi, e)
+                run_block(slot, pos)
+        p_tile = np.array([p_new[int(e)] for e in tpos], np.float32)
+        q, s = OF.fp8_tile(p_tile)
+        assert_bits_equal(f"fp8 codes tile {tslot}", got["fp8"][tpos], q)
+        assert_bits_equal(f"fp8 scale tile {tslot}", got["fs"][tslot:tslot + 1], np.array([s], np.float32))
+        assert_bits_equal(f"fp8 codes tile {tslot} (standalone)", got["q2"][tpos], q)
+        done += 1
+    assert done > 0

@@ -193,3 +193,25 @@ def test_golden_layouts_unchanged():
         L = P.plan(_descs(u), c.V, c.alpha, c.start_align)
         assert (L.S, len(L.intervals), L.n_mslots, L.n_fslots, L.starts) == \
             (w["S"], w["NI"], w["n_mslots"], w["n_fslots"], w["starts"]), key
+
+
+@pytest.mark.parametrize("name,dev", [("gptoss-small", (0, 8)), ("llama-tile-small", (1, 3)), ("toy", (2, 4))])
+def test_block_at_agrees_with_enumeration(name, dev):
+    """block_at (used to sample full-size outputs) finds the same slot and
+    positions as the full enumeration, for every block and tile."""
+    c = W.config(name)
+    L = P.plan(_descs(c.units[0]), c.V, c.alpha, c.start_align)
+    lo, hi = dev
+    rng = np.random.default_rng(1)
+    for fp8 in (False, True):
+        gen = P.fp8_tiles(L, lo, hi) if fp8 else P.adam_blocks(L, lo, hi)
+        for slot, pos in gen:
+            probe = int(pos[rng.integers(0, pos.size)])
+            got = P.block_at(L, lo, hi, probe, fp8=fp8)
+            assert got is not None and got[0] == slot and np.array_equal(np.sort(got[1]), np.sort(pos))
+    # padding positions belong to no block
+    covered = np.zeros((hi - lo) * L.S, bool)
+    for _, pos in P.adam_blocks(L, lo, hi):
+        covered[pos] = True
+    for probe in np.nonzero(~covered)[0][:50]:
+        assert P.block_at(L, lo, hi, int(probe)) is None
