@@ -49,31 +49,30 @@ __device__ __forceinline__ Hp make_hp(const bq_adam_hp& h) {
   return Hp{h.lr, h.b1, h.b2, h.eps, h.omb1, h.omb2, h.rbc1, h.rbc2};
 }
 
-// Blackwell's packed fp32 pair multiply: each component is rounded exactly like
-// the scalar round-to-nearest multiply.  Additions stay scalar (__fadd_rn):
-// ptxas contracts a packed multiply feeding a packed add into a fused
-// multiply-add even when both carry an explicit .rn, which would change results;
-// a scalar .rn add is never contracted.
+// Blackwell's packed fp32 pair arithmetic: each component is rounded exactly
+// like the scalar round-to-nearest operation.  A packed add takes no product as
+// an operand anywhere below: ptxas contracts a packed multiply feeding a packed
+// add into a fused multiply-add even when both carry an explicit .rn, so every
+// multiply-then-add is written as the explicit fused operation the contract
+// specifies.
 __device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 add2s(float2 a, float2 b) {
-  return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
-}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }  // operands never products
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-// The Adam update of two elements; per element, every step one IEEE fp32 op
-// rounded to nearest, no FMA:
-//   m' = b1*m + omb1*g;  v' = b2*v + omb2*(g*g);  mh = m'*rbc1;  vh = v'*rbc2;
-//   p' = p - lr*(mh/(sqrt(vh)+eps))
+// The Adam update of two elements; per element, each step one IEEE fp32
+// operation rounded to nearest, fma(x, y, z) = x*y + z rounded once:
+//   m' = fma(b1, m, omb1*g);  v' = fma(b2, v, omb2*(g*g));  mh = m'*rbc1;
+//   vh = v'*rbc2;  u = mh/(sqrt(vh)+eps);  p' = fma(-lr, u, p)
 __device__ __forceinline__ void adam_pair(const Hp& h, float2 g, float2 p, float2 qm, float2 qv, float2 sm, float2 sv,
                                           float2& p1, float2& m1, float2& v1) {
   const float2 m = mul2(qm, sm), v = mul2(qv, sv);
-  m1 = add2s(mul2(dup(h.b1), m), mul2(dup(h.omb1), g));
-  v1 = add2s(mul2(dup(h.b2), v), mul2(dup(h.omb2), mul2(g, g)));
+  m1 = fma2(dup(h.b1), m, mul2(dup(h.omb1), g));
+  v1 = fma2(dup(h.b2), v, mul2(dup(h.omb2), mul2(g, g)));
   const float2 mh = mul2(m1, dup(h.rbc1)), vh = mul2(v1, dup(h.rbc2));
-  const float2 den = add2s(make_float2(__fsqrt_rn(vh.x), __fsqrt_rn(vh.y)), dup(h.eps));
+  const float2 den = add2(make_float2(__fsqrt_rn(vh.x), __fsqrt_rn(vh.y)), dup(h.eps));
   const float2 u = make_float2(__fdiv_rn(mh.x, den.x), __fdiv_rn(mh.y, den.y));
-  const float2 lu = mul2(dup(h.lr), u);
-  p1 = make_float2(__fsub_rn(p.x, lu.x), __fsub_rn(p.y, lu.y));
+  p1 = fma2(dup(-h.lr), u, p);
 }
 
 // Block scale from an absmax (fp32 bits; all values >= 0 so bit order == value
@@ -99,12 +98,13 @@ __device__ __forceinline__ QScale qscale(uint32_t amax_bits, float qmax) {
 //    is the float 2^23 + b, so subtracting 2^23 gives float(b) exactly (a signed
 //    byte is first offset by 128 by flipping its top bit);
 //  * for |y| < 2^22, y + 1.5*2^23 rounds y to the nearest integer, ties to even
-//    (the add's own rounding), and the low byte of the sum's bit pattern is that
+//    (the add's own rounding; with y = x*r inside one fused multiply-add the
+//    exact product is rounded), and the low byte of the sum's bit pattern is that
 //    integer modulo 256 (two's complement for negative values).
 __device__ __forceinline__ float2 byte_pair(uint32_t w, int i, float bias) {
   const float2 t = make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | uint32_t(i))),
                                __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | uint32_t(i + 1))));
-  return add2s(t, dup(-bias));
+  return add2(t, dup(-bias));
 }
 
 // low bytes of four words -> one word
@@ -113,9 +113,10 @@ __device__ __forceinline__ uint32_t low_bytes(uint32_t a, uint32_t b, uint32_t c
 }
 
 // 8 int8 codes, packed little-endian into two words.  On the reciprocal path
-// |x * r| <= 127 (1 + 2^-23) because |x| <= amax, so the rounded value already
-// lies in [-127, 127] and needs no clamp; the division path (tiny blocks, whose
-// subnormal scale may be inexact) clamps.
+// fma(x, r, 1.5*2^23) = 1.5*2^23 + rint(x*r) with the exact product rounded once
+// to an integer; |x * r| <= 127 (1 + 2^-23) because |x| <= amax, so that integer
+// already lies in [-127, 127] and needs no clamp.  The division path (tiny
+// blocks, whose subnormal scale may be inexact) rounds x/s and clamps.
 __device__ __forceinline__ uint2 codes_int8(const float* x, const QScale& q) {
   if (q.mode == 0) return make_uint2(0u, 0u);
   uint32_t b[8];
@@ -123,7 +124,7 @@ __device__ __forceinline__ uint2 codes_int8(const float* x, const QScale& q) {
     const float2 r = dup(q.r), k = dup(12582912.f);
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
-      const float2 y = add2s(mul2(make_float2(x[i], x[i + 1]), r), k);
+      const float2 y = fma2(make_float2(x[i], x[i + 1]), r, k);  // K + rint(x*r), the product unrounded
       b[i] = __float_as_uint(y.x);
       b[i + 1] = __float_as_uint(y.y);
     }
@@ -143,7 +144,7 @@ __device__ __forceinline__ uint2 codes_uint8(const float* x, const QScale& q) {
     const float2 r = dup(q.r), k = dup(8388608.f);
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
-      const float2 y = add2s(mul2(make_float2(x[i], x[i + 1]), r), k);
+      const float2 y = fma2(make_float2(x[i], x[i + 1]), r, k);
       b[i] = __float_as_uint(y.x);
       b[i + 1] = __float_as_uint(y.y);
     }
@@ -442,7 +443,7 @@ __device__ __forceinline__ void store_state(const AdamArgs& a, int64_t pos, int 
 template <int E>
 __global__ void __launch_bounds__(kThreads, kAdamCtas) k_flat(const FlatGroup* __restrict__ groups, AdamArgs a) {
   constexpr int B = 32 * E;
-  const FlatGroup g = groups[blockIdx.x];
+  const FlatGroup g = groups[gridDim.x - 1 - blockIdx.x];  // back to front, see k_strip
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Hp h = make_hp(a.hp);
   const int nblk = (g.nelem + B - 1) / B;
@@ -477,7 +478,9 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_flat(const FlatGroup* _
 }
 
 // ---------------------------------------------------------------- flat 256 Adam + 2-D FP8 tiles
-// One CTA per region (grid-stride).  Phase 1: warps run Adam over the region's
+// One CTA per region (grid-stride, last region first: the pack that precedes
+// this step writes the gradient buffer front to back, so its tail is still in
+// L2 when this kernel starts).  Phase 1: warps run Adam over the region's
 // 256-element blocks, write state and master, and fold |p'| into per-column-tile
 // maxima in shared memory.  Phase 2: tile scales, then the updated master is
 // re-read (it was written moments ago by this CTA and is served from L2) and
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_strip(const RegionGroup
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Hp h = make_hp(a.hp);
   StageBuf* st = pipe + warp * kStages;
-  for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
+  for (int gi = ngroups - 1 - int(blockIdx.x); gi >= 0; gi -= int(gridDim.x)) {
     const RegionGroup g = groups[gi];
     // strip: rows x 256 columns, block = one row segment; band: rows x C,
     // flat 256-element blocks from the band start
@@ -635,7 +638,7 @@ template <bool FP8>
 __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
   __shared__ uint32_t red[3 * kWarps];
   const Hp h = make_hp(a.hp);
-  for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
+  for (int gi = ngroups - 1 - int(blockIdx.x); gi >= 0; gi -= int(gridDim.x)) {
     const RegionGroup g = groups[gi];
     const bool fp8 = FP8 && g.fslot >= 0;
     const float sm = a.m_scale[g.mslot], sv = a.v_scale[g.mslot];

@@ -164,15 +164,16 @@ int bq_pack(const bq_shard* shard, const void* const* grad_ptrs, void* dbuf_grad
  * Defined by: 8-bit Adam with per-block quantised state kept device-local by
  * RaggedShard granularity (bud-325 summary, Key claims; feynmanwiki walkthrough,
  * paper section 6.3) and block-wise FP8 (DeepSeek-V3 style, bud-325 TL;DR).
- * Per element, each an IEEE fp32 op rounded to nearest, no FMA:
- *   g=f32(grad); m=qm*sm; v=qv*sv; m'=b1*m+omb1*g; v'=b2*v+omb2*(g*g);
- *   p'=p-lr*((m'*rbc1)/(sqrt(v'*rbc2)+eps))
- * per Adam block: sm'=max|m'|/127, qm'=clamp(rint(m'*(127/max|m'|)),-127,127);
- *   sv'=max v'/255, qv'=clamp(rint(v'*(255/max v')),0,255) (the reciprocal is
- *   one fp32 division per block; if it overflows, m'/sm' resp. v'/sv' is used);
+ * Per element, each an IEEE fp32 op rounded to nearest; fma = one rounding:
+ *   g=f32(grad); m=qm*sm; v=qv*sv; m'=fma(b1,m,omb1*g); v'=fma(b2,v,omb2*(g*g));
+ *   u=(m'*rbc1)/(sqrt(v'*rbc2)+eps); p'=fma(-lr,u,p)
+ * per Adam block: sm'=max|m'|/127, qm'=clamp(rint(m'*(127/max|m'|)),-127,127)
+ *   with the product rounded once, directly to an integer; sv'=max v'/255,
+ *   qv'=clamp(rint(v'*(255/max v')),0,255) likewise (each reciprocal is one fp32
+ *   division per block; if it overflows, rint(fp32(m'/sm')) resp. v'/sv');
  *   a block whose scale is 0 gets zero codes.
  * per FP8 tile (if fp8_out != NULL): s=max|p'|/448, code=e4m3_rne_satfinite(
- *   p'*(448/max|p'|)) (p'/s if the reciprocal overflows); scale 0 -> codes +-0.
+ *   fp32(p'*(448/max|p'|))) (p'/s if the reciprocal overflows); scale 0 -> +-0.
  * grad: bf16 packed buffer; master fp32, m int8, v uint8, fp8_out uint8 - all
  * (dev_hi-dev_lo)*S elements, updated in place (padding untouched); m_scale,
  * v_scale: fp32 per Adam slot; fp8_scale: fp32 per FP8 slot (a scale buffer may

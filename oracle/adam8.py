@@ -14,12 +14,12 @@ Readings (the pages give neither the update nor the quantiser):
   * m is stored as int8 codes in [-127, 127] and v as uint8 codes, each block with
     one fp32 absmax scale (linear map, see codecs.quant_*_absmax);
   * the per-element order of operations is fixed, each step one IEEE fp32
-    operation rounded to nearest, no fused multiply-add:
+    operation rounded to nearest; fma(x, y, z) = x*y + z rounded once:
         g   = f32(bf16 grad)
         m   = code_m * s_m            v   = code_v * s_v
-        m'  = b1*m + omb1*g           v'  = b2*v + omb2*(g*g)
+        m'  = fma(b1, m, omb1*g)      v'  = fma(b2, v, omb2*(g*g))
         mh  = m' * rbc1               vh  = v' * rbc2
-        p'  = p - lr * (mh / (sqrt(vh) + eps))
+        u   = mh / (sqrt(vh) + eps)   p'  = fma(-lr, u, p)
     with omb1 = 1-b1, omb2 = 1-b2 and the reciprocal bias corrections
     rbc1 = 1/(1-b1^t), rbc2 = 1/(1-b2^t) evaluated in fp64 and rounded once to
     fp32 (adam_hparams);
@@ -29,7 +29,7 @@ Readings (the pages give neither the update nor the quantiser):
 
 import numpy as np
 
-from .codecs import bf16_bits_to_f32, dequant, quant_int8_absmax, quant_uint8_absmax
+from .codecs import bf16_bits_to_f32, dequant, fma32, quant_int8_absmax, quant_uint8_absmax
 from .planner import adam_blocks
 
 F32 = np.float32
@@ -47,11 +47,12 @@ def adam_update(g_bits, p, m, v, hp):
     """Elementwise fp32 Adam update from dequantised state.  Returns (p', m', v')."""
     g = bf16_bits_to_f32(g_bits)
     p = np.asarray(p, dtype=np.float32)
-    m1 = hp["b1"] * m + hp["omb1"] * g
-    v1 = hp["b2"] * v + hp["omb2"] * (g * g)
+    m1 = fma32(hp["b1"], m, hp["omb1"] * g)
+    v1 = fma32(hp["b2"], v, hp["omb2"] * (g * g))
     mh = m1 * hp["rbc1"]
     vh = v1 * hp["rbc2"]
-    p1 = p - hp["lr"] * (mh / (np.sqrt(vh) + hp["eps"]))
+    u = mh / (np.sqrt(vh) + hp["eps"])
+    p1 = fma32(-hp["lr"], u, p)
     return p1.astype(np.float32), m1.astype(np.float32), v1.astype(np.float32)
 
 

@@ -11,7 +11,9 @@
 * int8 / uint8 linear absmax block quantisers for the 8-bit Adam state ("8-bit
   Adam" in Key claims; the pages give block locality but no quantiser, so the
   reading is a symmetric linear map with one fp32 absmax scale per block; codes
-  are formed by multiplying with the reciprocal scale, computed once per block).
+  are the product with the reciprocal scale, computed once per block, rounded
+  once to an integer).
+* fma32: the fp32 fused multiply-add (one rounding), used by the Adam update.
 
 Everything is numpy; fp32 arithmetic is done on float32 arrays so that every
 operation is one IEEE fp32 operation rounded to nearest.
@@ -40,6 +42,37 @@ def f32_to_bf16_bits(x):
 def bf16_bits_to_f32(b):
     """bf16 bit pattern -> the fp32 value it denotes (exact)."""
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ----------------------------------------------------------------------------- fused multiply-add
+
+
+def fma32(a, b, c):
+    """fp32 fused multiply-add: a*b + c rounded once to nearest-even fp32.
+
+    The product of two fp32 numbers is exact in fp64; the fp64 sum s = a*b + c
+    is corrected by its exact error e (Knuth's TwoSum: s + e == a*b + c).  The
+    fp64 rounding of s can only matter when s falls exactly on a midpoint between
+    two fp32 numbers: any other s lies at least one fp64 ulp from every fp32
+    midpoint while |e| is at most half an fp64 ulp.  At such a midpoint the sign
+    of e decides (e == 0 is a true tie: nearest even)."""
+    a64 = np.asarray(a, np.float32).astype(np.float64)
+    b64 = np.asarray(b, np.float32).astype(np.float64)
+    c64 = np.asarray(c, np.float32).astype(np.float64)
+    p = a64 * b64
+    s = p + c64
+    bp = s - p
+    e = (p - (s - bp)) + (c64 - bp)
+    with np.errstate(over="ignore", invalid="ignore"):
+        r = s.astype(np.float32)
+        r64 = r.astype(np.float64)
+        up = np.nextafter(r, np.float32(np.inf))
+        dn = np.nextafter(r, np.float32(-np.inf))
+        lo = np.where(r64 < s, r, dn)
+        hi = np.where(r64 < s, up, r)
+        mid = (lo.astype(np.float64) + hi.astype(np.float64)) / 2 == s
+    tie_break = mid & (r64 != s) & (e != 0)
+    return np.where(tie_break, np.where(e > 0, hi, lo), r).astype(np.float32)
 
 
 # ----------------------------------------------------------------------------- FP8 E4M3
@@ -125,34 +158,42 @@ def scaled(x, s, r, mode):
     return x * r if mode == 1 else x / s
 
 
+def rint_product(x, r):
+    """rint of the exact product x*r (fp32 x, fp32 r), ties to even: the fp64
+    product is exact and fp64 rint is exact."""
+    return np.rint(np.asarray(x, np.float32).astype(np.float64) * np.float64(np.float32(r)))
+
+
 def quant_int8_absmax(x):
     """One block of signed state -> (int8 codes, fp32 scale).
 
-    s = max|x| / 127 is the stored scale; the codes use the reciprocal
-    r = 127 / max|x| (one fp32 division per block): code = clamp(rint(x * r),
-    -127, 127), rint = half-to-even (x / s when r overflows, see block_scale).
-    A block whose scale is 0 gets zero codes; -128 is never produced."""
+    s = max|x| / 127 is the stored scale; with the reciprocal r = 127 / max|x|
+    (one fp32 division per block) code = clamp(rint(x * r), -127, 127) where the
+    product is rounded once, directly to an integer (half to even); when r
+    overflows, code = clamp(rint(fp32(x / s))).  A block whose scale is 0 gets
+    zero codes; -128 is never produced."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     amax = np.max(np.abs(x)) if x.size else F32(0)
     s, r, mode = block_scale(amax, 127)
     if mode == 0:
         return np.zeros(x.shape, np.int8), F32(0)
-    q = np.clip(np.rint(scaled(x, s, r, mode)), -127, 127)
-    return q.astype(np.int8), s
+    y = rint_product(x, r) if mode == 1 else np.rint(x / s)
+    return np.clip(y, -127, 127).astype(np.int8), s
 
 
 def quant_uint8_absmax(x):
     """One block of non-negative state -> (uint8 codes, fp32 scale).
 
-    s = max x / 255; code = clamp(rint(x * r), 0, 255) with r = 255 / max x
-    (x / s when r overflows); a block whose scale is 0 gets zero codes."""
+    s = max x / 255; code = clamp(rint(x * r), 0, 255) with r = 255 / max x and
+    the product rounded once to an integer (x / s when r overflows); a block
+    whose scale is 0 gets zero codes."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     amax = np.max(x) if x.size else F32(0)
     s, r, mode = block_scale(amax, 255)
     if mode == 0:
         return np.zeros(x.shape, np.uint8), F32(0)
-    q = np.clip(np.rint(scaled(x, s, r, mode)), 0, 255)
-    return q.astype(np.uint8), s
+    y = rint_product(x, r) if mode == 1 else np.rint(x / s)
+    return np.clip(y, 0, 255).astype(np.uint8), s
 
 
 def dequant(codes, scale):

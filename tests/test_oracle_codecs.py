@@ -143,3 +143,59 @@ def test_tiny_blocks_take_the_division_or_zero_path():
     assert s3 == 0 and not q.any()
     # ordinary block: reciprocal path
     assert C.block_scale(np.float32(2.0), 127)[2] == 1
+
+
+def _rn_f32_exact(q):
+    """Nearest-even binary32 to the rational q (exact reference, slow)."""
+    from fractions import Fraction
+
+    if q == 0:
+        return np.float32(0.0)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -126) - 23)
+    k = a / quantum
+    n = k.numerator // k.denominator
+    rem = k - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return np.float32(sign * float(n * quantum))
+
+
+def test_fma32_against_exact_rationals():
+    from fractions import Fraction
+
+    rng = np.random.default_rng(12)
+    a = (rng.standard_normal(6000) * 10.0 ** rng.integers(-8, 8, 6000)).astype(np.float32)
+    b = (rng.standard_normal(6000) * 10.0 ** rng.integers(-8, 8, 6000)).astype(np.float32)
+    c = (rng.standard_normal(6000) * 10.0 ** rng.integers(-8, 8, 6000)).astype(np.float32)
+    # heavy cancellation: c close to -a*b
+    c[:2000] = (-(a[:2000].astype(np.float64) * b[:2000]) * (1 + rng.standard_normal(2000) * 1e-7)).astype(np.float32)
+    got = C.fma32(a, b, c)
+    for i in range(a.size):
+        want = _rn_f32_exact(Fraction(float(a[i])) * Fraction(float(b[i])) + Fraction(float(c[i])))
+        assert got[i].view(np.uint32) == want.view(np.uint32), (a[i], b[i], c[i], got[i], want)
+
+
+def test_fma32_double_rounding_case():
+    """a*b + c = 1 + 2^-23 + 2^-24 - 2^-70: just below the midpoint between
+    1 + 2^-23 and 1 + 2^-22, so the answer is 1 + 2^-23; rounding to fp64 first
+    would land on the midpoint and round to even (1 + 2^-22)."""
+    a = np.float32(1 + 2.0 ** -23)
+    b = np.float32(2.0 ** -24 * (1 - 2.0 ** -23))
+    c = np.float32(1 + 2.0 ** -23)
+    assert C.fma32(a, b, c) == np.float32(1 + 2.0 ** -23)
+    assert np.float32(np.float64(a) * np.float64(b) + np.float64(c)) == np.float32(1 + 2.0 ** -22)
+    assert C.fma32(-a, b, -c) == -np.float32(1 + 2.0 ** -23)
+
+
+def test_fma32_without_addend_is_the_rounded_product():
+    rng = np.random.default_rng(13)
+    a = rng.standard_normal(100000).astype(np.float32)
+    b = rng.standard_normal(100000).astype(np.float32)
+    assert np.array_equal(C.fma32(a, b, np.zeros_like(a)).view(np.uint32), (a * b).view(np.uint32))
