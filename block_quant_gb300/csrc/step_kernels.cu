@@ -310,7 +310,7 @@ __device__ __forceinline__ void stage_issue(StageBuf& sb, int lane, const AdamAr
   cp_async8(&sb.v[lane], a.v + pos);
 }
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;  // three blocks per warp in flight while one is computed
 
 // ---------------------------------------------------------------- Adam over one 8-element lane slice
 // The lane's inputs stay packed (bf16 pairs, fp32 quads, code bytes) and are
