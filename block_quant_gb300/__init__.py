@@ -23,7 +23,7 @@ ADAM_FLAT256, ADAM_TILE128 = 0, 1
 # every entry point include/bq.h declares
 SYMBOLS = [
     "bq_strerror", "bq_last_error", "bq_version", "bq_plan", "bq_layout_free", "bq_layout_query",
-    "bq_layout_export", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_pack",
+    "bq_layout_export", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_shard_check", "bq_pack",
     "bq_step_adam8", "bq_quant_fp8", "bq_muon_ns_workspace", "bq_muon_ns", "bq_muon_ns_check",
     "bq_muon_ns_noalloc",
 ]
@@ -92,6 +92,7 @@ def load():
     lib.bq_muon_ns.argtypes = [C.c_int, C.POINTER(Mat), C.c_int, C.c_float, C.c_float, C.c_float, C.c_float,
                                P, C.c_size_t, P]
     lib.bq_muon_ns_check.argtypes = [P, C.c_size_t, P]
+    lib.bq_shard_check.argtypes = [P, P]
     lib.bq_muon_ns_noalloc.argtypes = [C.c_int, C.POINTER(Mat), C.c_int, C.c_float, C.c_float, C.c_float,
                                        C.c_float, P]
     for name in SYMBOLS:
@@ -253,6 +254,12 @@ def muon_ns(mats, ws, ws_bytes=None, steps=5, a=3.4445, b=-4.7750, c=2.0315, eps
         ws_bytes = ws.numel() * ws.element_size()
     _check(load().bq_muon_ns(len(arr), arr, int(steps), float(a), float(b), float(c), float(eps), _ptr(ws),
                              int(ws_bytes), _stream(stream)))
+
+
+def shard_check(shard, stream=None):
+    """Synchronise the stream and raise if a device wait of an Adam step on this
+    shard timed out since the last check."""
+    _check(load().bq_shard_check(shard.handle, _stream(stream)))
 
 
 def muon_ns_check(ws, ws_bytes=None, stream=None):

@@ -51,7 +51,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsPlan {
-  size_t off_pieces, off_chunks, off_f256, off_f128, off_strips, off_tiles, bytes;
+  size_t off_pieces, off_chunks, off_f256, off_f128, off_strips, off_tiles, off_status, bytes;
 };
 
 WsPlan ws_plan(const ShardTables& T) {
@@ -69,7 +69,9 @@ WsPlan ws_plan(const ShardTables& T) {
   o = align_up(o + T.strips.size() * sizeof(RegionGroup), 256);
   p.off_tiles = o;
   o = align_up(o + T.tiles.size() * sizeof(RegionGroup), 256);
-  p.bytes = std::max<size_t>(o, 256);
+  p.off_status = o;  // device error word, zeroed by the upload
+  o += 256;
+  p.bytes = o;
   return p;
 }
 
@@ -166,6 +168,7 @@ int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, s
   sh->dev.n_strips = int32_t(T.strips.size());
   sh->dev.n_tiles = int32_t(T.tiles.size());
   sh->dev.max_strip_tiles = T.max_strip_tiles;
+  sh->dev.status = reinterpret_cast<int*>(base + p.off_status);
   *out = sh;
   return BQ_OK;
 }
@@ -196,7 +199,8 @@ int bq_step_adam8(const bq_shard* sh, const void* grad, float* master, int8_t* m
   if ((reinterpret_cast<uintptr_t>(m_scale) | reinterpret_cast<uintptr_t>(v_scale) |
        reinterpret_cast<uintptr_t>(fp8_scale)) & 3)
     return set_error(BQ_EALIGN, "bq_step_adam8: scale buffers must be 4-byte aligned");
-  AdamArgs a{static_cast<const uint16_t*>(grad), master, m, v, m_scale, v_scale, fp8_out, fp8_scale, *hp};
+  AdamArgs a{static_cast<const uint16_t*>(grad), master, m, v, m_scale, v_scale, fp8_out, fp8_scale, *hp,
+             sh->dev.status};
   return launch_adam8(sh->dev, a, stream);
 }
 
@@ -206,6 +210,19 @@ int bq_quant_fp8(const bq_shard* sh, const float* master, uint8_t* fp8_out, floa
   if (!aligned16(master) || !aligned16(fp8_out) || (reinterpret_cast<uintptr_t>(fp8_scale) & 3))
     return set_error(BQ_EALIGN, "bq_quant_fp8: misaligned buffer");
   return launch_quant_fp8(sh->dev, master, fp8_out, fp8_scale, stream);
+}
+
+int bq_shard_check(const bq_shard* sh, bq_stream_t stream) {
+  if (!sh) return set_error(BQ_EINVAL, "bq_shard_check: shard is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int status = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&status, sh->dev.status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && status) e = cudaMemset(sh->dev.status, 0, sizeof(int));
+  if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string("bq_shard_check: ") + cudaGetErrorString(e));
+  if (status)
+    return set_error(BQ_ECUDA, "bq_step_adam8: a device wait timed out (site " + std::to_string(status) + ")");
+  return BQ_OK;
 }
 
 int bq_muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes) { return muon_ns_workspace(batch, mats, bytes); }

@@ -117,6 +117,7 @@ struct DevTables {
   int64_t nchunks;
   int32_t n_flat256, n_flat128, n_strips, n_tiles;
   int32_t max_strip_tiles;
+  int* status;  // device error word: 0, or the site of a wait that timed out
 };
 
 struct AdamArgs {
@@ -129,6 +130,7 @@ struct AdamArgs {
   uint8_t* fp8;      // may be null
   float* fp8_scale;  // may be null
   bq_adam_hp hp;
+  int* status;  // device error word of the shard (set by the launcher)
 };
 
 int launch_pack(const DevTables& t, const uint16_t* const* grads, uint16_t* dst, int64_t total, float scale,

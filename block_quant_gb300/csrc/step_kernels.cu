@@ -79,6 +79,14 @@ __device__ __forceinline__ void adam_pair(const Hp& h, float2 g, float2 p, float
 // order): stored scale s = amax/qmax, reciprocal r = qmax/amax (one division each
 // per block).  mode 0: s == 0 -> zero codes; 1: codes from x*r; 2: r overflowed
 // (tiny amax) -> codes from x/s.
+// max of three floats; a NaN operand gives NaN (so a NaN in a block reaches its
+// scale, as a maximum over the raw bit patterns would)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 struct QScale {
   float s, r;
   int mode;
@@ -256,61 +264,72 @@ __global__ void __launch_bounds__(kThreads) k_pack(const PackPiece* __restrict__
   }
 }
 
-// ---------------------------------------------------------------- asynchronous staging
-// A warp streams its Adam blocks through a few shared-memory stages filled with
-// cp.async, so that several blocks' loads are in flight per warp with few
-// registers.  Each lane reads back only the bytes it copied itself.
+// ---------------------------------------------------------------- TMA staging
+// The 2-D Adam kernel streams its inputs through shared memory with bulk
+// asynchronous copies issued by one producer warp (the copy engine moves whole
+// row segments, so many kilobytes per SM are in flight without load
+// instructions or registers); completion is tracked by mbarriers.  Every wait is
+// bounded: after about a second it records a status code and gives up.
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-
-// one stage of one warp: the 8-element slices of 32 lanes, lane-contiguous
-struct StageBuf {
-  uint4 g[32];
-  float4 p0[32], p1[32];
-  uint2 m[32], v[32];
-  float sc[4];  // the block's m and v scales (staged by lanes 0 and 1)
-};
-
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-// lanes 0 and 1 stage the block's two scales
-__device__ __forceinline__ void stage_scales(StageBuf& sb, int lane, const AdamArgs& a, int slot) {
-  if (lane == 0) cp_async4(&sb.sc[0], a.m_scale + slot);
-  if (lane == 1) cp_async4(&sb.sc[1], a.v_scale + slot);
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared.b64 [%0], %1;\n" ::"r"(smem_u32(b)), "r"(count) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared.b64 _, [%0];\n" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;\n" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+
+// one arrival on b once every earlier cp.async of this thread has landed
+__device__ __forceinline__ void mbar_arrive_cp_async(uint64_t* b) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];\n" ::"r"(smem_u32(b)) : "memory");
+}
+
+constexpr long long kWaitCycles = 1LL << 31;  // about a second at the SM clock
+
+// wait for the completion of the phase of b with the given parity; false on timeout
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+
+// bulk copy global -> this CTA's shared memory, completion counted on bar
+// (addresses 16-byte aligned, bytes a multiple of 16)
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void report(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// n / d by multiply-high and shift (mul, shr from the host; mul == 0: d == 1)
 __device__ __forceinline__ uint32_t fastdiv(uint32_t n, uint32_t mul, uint32_t shr) {
   return mul ? (__umulhi(n, mul) >> shr) : n;
 }
-
-__device__ __forceinline__ void stage_issue(StageBuf& sb, int lane, const AdamArgs& a, int64_t pos) {
-  cp_async16(&sb.g[lane], a.grad + pos);
-  cp_async16(&sb.p0[lane], a.master + pos);
-  cp_async16(&sb.p1[lane], a.master + pos + 4);
-  cp_async8(&sb.m[lane], a.m + pos);
-  cp_async8(&sb.v[lane], a.v + pos);
-}
-
-constexpr int kStages = 4;  // three blocks per warp in flight while one is computed
 
 // ---------------------------------------------------------------- Adam over one 8-element lane slice
 // The lane's inputs stay packed (bf16 pairs, fp32 quads, code bytes) and are
@@ -321,16 +340,6 @@ struct Raw8 {
   float4 p0, p1;
   uint2 m, v;
 };
-
-__device__ __forceinline__ Raw8 raw_from_stage(const StageBuf& sb, int lane) {
-  Raw8 r;
-  r.g = sb.g[lane];
-  r.p0 = sb.p0[lane];
-  r.p1 = sb.p1[lane];
-  r.m = sb.m[lane];
-  r.v = sb.v[lane];
-  return r;
-}
 
 __device__ __forceinline__ Raw8 raw_from_global(const AdamArgs& a, int64_t pos, int n) {
   Raw8 r;
@@ -369,7 +378,6 @@ struct Lane8 {
 
 template <bool FULL>
 __device__ __forceinline__ void adam_raw(const Hp& h, const Raw8& x, int n, float sm, float sv, Lane8& o) {
-  o.am = o.av = o.ap = 0u;
   const uint32_t gw[4] = {x.g.x, x.g.y, x.g.z, x.g.w};
   const float pv[8] = {x.p0.x, x.p0.y, x.p0.z, x.p0.w, x.p1.x, x.p1.y, x.p1.z, x.p1.w};
   const uint32_t mw[2] = {x.m.x ^ 0x80808080u, x.m.y ^ 0x80808080u}, vw[2] = {x.v.x, x.v.y};
@@ -388,14 +396,19 @@ __device__ __forceinline__ void adam_raw(const Hp& h, const Raw8& x, int n, floa
     o.v1[2 * j] = v1.x;
     o.v1[2 * j + 1] = v1.y;
   }
+  // lane maxima of |m'|, v' (>= 0) and |p'|, three operands per max; elements
+  // past n count as 0
+  float am = 0.f, av = 0.f, ap = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (FULL || i < n) {
-      o.am = max(o.am, __float_as_uint(fabsf(o.m1[i])));
-      o.av = max(o.av, __float_as_uint(o.v1[i]));
-      o.ap = max(o.ap, __float_as_uint(fabsf(o.p1[i])));
-    }
+  for (int i = 0; i < 8; i += 2) {
+    const bool a0 = FULL || i < n, a1 = FULL || i + 1 < n;
+    am = max3(am, a0 ? fabsf(o.m1[i]) : 0.f, a1 ? fabsf(o.m1[i + 1]) : 0.f);
+    av = max3(av, a0 ? o.v1[i] : 0.f, a1 ? o.v1[i + 1] : 0.f);
+    ap = max3(ap, a0 ? fabsf(o.p1[i]) : 0.f, a1 ? fabsf(o.p1[i + 1]) : 0.f);
   }
+  o.am = __float_as_uint(am);
+  o.av = __float_as_uint(av);
+  o.ap = __float_as_uint(ap);
 }
 
 // Block scales of m' and v' from the lanes' partial maxima: lane 0 computes the
@@ -466,10 +479,8 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_flat(const FlatGroup* _
       a.v_scale[slot] = qv.s;
     }
     if (do_fp8) {
-      uint32_t ap = o.ap;
       // reduce over the lanes of one 128-element tile: 16 lanes (E = 8) or 32 (E = 4)
-#pragma unroll
-      for (int off = (E == 8 ? 8 : 16); off >= 1; off >>= 1) ap = max(ap, __shfl_xor_sync(0xFFFFFFFFu, ap, off));
+      const uint32_t ap = __reduce_max_sync(E == 4 ? 0xFFFFFFFFu : (lane < 16 ? 0x0000FFFFu : 0xFFFF0000u), o.ap);
       const QScale qp = qscale(ap, 448.f);
       store_bytes(a.fp8 + pos, codes_e4m3(o.p1, qp), n);
       if ((e0 & 127) == 0 && e0 < g.nelem) a.fp8_scale[g.fslot + e0 / 128] = qp.s;
@@ -478,75 +489,202 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_flat(const FlatGroup* _
 }
 
 // ---------------------------------------------------------------- flat 256 Adam + 2-D FP8 tiles
-// One CTA per region (grid-stride, last region first: the pack that precedes
-// this step writes the gradient buffer front to back, so its tail is still in
-// L2 when this kernel starts).  Phase 1: warps run Adam over the region's
-// 256-element blocks, write state and master, and fold |p'| into per-column-tile
-// maxima in shared memory.  Phase 2: tile scales, then the updated master is
-// re-read (it was written moments ago by this CTA and is served from L2) and
-// converted to E4M3.  Shared memory: 2 words per column tile.
+// Regions (128-row x 256-column strips, or whole 128-row bands when C % 256 != 0)
+// are taken by CTAs in a grid-stride loop, last region first (the pack that
+// precedes this step writes the gradient buffer front to back, so its tail is
+// still in L2 when this kernel starts).  Warp kCons is the producer: it fills a
+// ring of kRing shared-memory stages, each with the next kCons Adam blocks (one
+// bulk copy per block and array; the blocks' two scales by cp.async), and runs
+// ahead across region boundaries.  Warps 0..kCons-1 consume one block each per
+// stage: Adam, state and master written back, |p'| folded into per-column-tile
+// maxima in shared memory.  After a region's last stage they compute the tile
+// scales and convert the region's updated master to E4M3, re-reading it (this
+// CTA wrote it moments ago, so it comes from L2).  A block is staged only when
+// it is whole and starts on a 16-byte boundary of the byte arrays; any other
+// block (a band's ragged tail) is read directly from global memory.
+
+#ifndef BQ_STRIP_CONSUMERS
+#define BQ_STRIP_CONSUMERS 8
+#endif
+constexpr int kCons = BQ_STRIP_CONSUMERS;        // consumer warps
+constexpr int kScaleLanes = 2 * kCons < 32 ? 2 * kCons : 32;  // producer lanes staging scales
+constexpr int kStripThreads = 32 * (kCons + 1);  // + the producer warp
+#ifndef BQ_STRIP_RING
+#define BQ_STRIP_RING 4
+#endif
+constexpr int kRing = BQ_STRIP_RING;             // stages in the ring
+#ifndef BQ_STRIP_CTAS_PER_SM
+#define BQ_STRIP_CTAS_PER_SM 3
+#endif
+constexpr int kStripCtas = BQ_STRIP_CTAS_PER_SM;
+
+struct TmaStage {
+  uint4 g[kCons][32];   // bf16 gradients, 512 B per block
+  float4 p[kCons][64];  // fp32 master, 1 KB per block
+  uint2 m[kCons][32];   // int8 m codes
+  uint2 v[kCons][32];   // uint8 v codes
+  float sc[2 * kCons];  // per block: m scale, v scale
+};
+static_assert(sizeof(TmaStage) % 16 == 0, "stages keep 16-byte alignment");
+constexpr uint32_t kBlockBytes = 512 + 1024 + 256 + 256;
+
+__device__ __forceinline__ int region_blocks(const RegionGroup& g) {
+  return g.width == g.C ? (g.rows * g.width + 255) >> 8 : g.rows;
+}
+
+// first element, element count and scale slot of Adam block b of region g
+// (strip: row b of the strip; band: flat 256-element block b from the band start)
+__device__ __forceinline__ void region_block(const RegionGroup& g, int b, int64_t& start, int& nel, int& slot) {
+  if (g.width == g.C) {
+    start = g.pos + (int64_t(b) << 8);
+    nel = min(256, g.rows * g.width - (b << 8));
+    slot = g.mslot + b;
+  } else {
+    start = g.pos + int64_t(b) * g.C;
+    nel = 256;
+    slot = g.mslot + b * (g.C >> 8);
+  }
+}
+
+__device__ __forceinline__ bool block_staged(int64_t start, int nel) { return nel == 256 && (start & 15) == 0; }
+
+// barrier of the consumer warps only (the producer never joins it)
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(32 * kCons) : "memory"); }
+
+__device__ __forceinline__ void strip_producer(const RegionGroup* __restrict__ groups, int ngroups, const AdamArgs& a,
+                                               TmaStage* ring, uint64_t* full, uint64_t* empty, int lane) {
+  uint32_t k = 0;  // stages issued
+  bool ok = true;
+  for (int gi = ngroups - 1 - int(blockIdx.x); ok && gi >= 0; gi -= int(gridDim.x)) {
+    const RegionGroup g = groups[gi];
+    const int nblk = region_blocks(g);
+    for (int j = 0; j < nblk; j += kCons, ++k) {
+      const int s = int(k % kRing);
+      if (k >= kRing) {
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ((k / kRing) - 1) & 1));
+        if (!ok) break;
+      }
+      TmaStage& S = ring[s];
+      // pass q, lane = 4 w + arr: array arr (g, p, m, v) of the stage's block 8 q + w
+      constexpr int kPasses = (kCons + 7) / 8;
+      bool staged[kPasses];
+      int64_t start[kPasses];
+      uint32_t nst = 0;
+#pragma unroll
+      for (int q = 0; q < kPasses; ++q) {
+        const int w = 8 * q + (lane >> 2);
+        int nel = 0, slot = 0;
+        start[q] = 0;
+        const bool have = w < kCons && j + w < nblk;
+        if (have) region_block(g, j + w, start[q], nel, slot);
+        staged[q] = have && block_staged(start[q], nel);
+        nst += __popc(__ballot_sync(0xFFFFFFFFu, staged[q] && (lane & 3) == 0));
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], nst * kBlockBytes);
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < kPasses; ++q) {
+        const int w = 8 * q + (lane >> 2), arr = lane & 3;
+        if (staged[q]) {
+          if (arr == 0) bulk_load(S.g[w], a.grad + start[q], 512, &full[s]);
+          else if (arr == 1) bulk_load(S.p[w], a.master + start[q], 1024, &full[s]);
+          else if (arr == 2) bulk_load(S.m[w], a.m + start[q], 256, &full[s]);
+          else bulk_load(S.v[w], a.v + start[q], 256, &full[s]);
+        }
+      }
+      // scale i (i & 1 ? v : m of block i >> 1) by lane i % 32
+      if (lane < kScaleLanes) {
+        for (int i = lane; i < 2 * kCons; i += 32) {
+          const int bb = j + (i >> 1);
+          if (bb < nblk) {
+            int64_t st2;
+            int ne2, sl2;
+            region_block(g, bb, st2, ne2, sl2);
+            cp_async4(&S.sc[i], ((i & 1) ? a.v_scale : a.m_scale) + sl2);
+          }
+        }
+        mbar_arrive_cp_async(&full[s]);
+      }
+    }
+  }
+  if (!ok && lane == 0) report(a.status, 1);
+  // no copy of this CTA may still be in flight when it exits
+  for (uint32_t d = k > uint32_t(kRing) ? k - kRing : 0; d < k; ++d)
+    if (!mbar_wait(&full[d % kRing], (d / kRing) & 1) && lane == 0) report(a.status, 2);
+}
 
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads, kAdamCtas) k_strip(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
-  // dynamic shared memory: the warps' staging pipes, then 2 words per FP8
-  // column tile ([ntile] amax bits, later r; [ntile..2*ntile) s)
-  extern __shared__ __align__(16) unsigned char s_dyn[];
-  StageBuf* pipe = reinterpret_cast<StageBuf*>(s_dyn);
-  uint32_t* s_tile = reinterpret_cast<uint32_t*>(s_dyn + sizeof(StageBuf) * kWarps * kStages);
+__global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const RegionGroup* __restrict__ groups, int ngroups,
+                                                                     AdamArgs a) {
+  // dynamic shared memory: the stage ring, its full / empty mbarriers, then 2
+  // words per FP8 column tile ([ntile] amax bits, later r; [ntile..2*ntile) s)
+  extern __shared__ __align__(128) unsigned char s_dyn[];
+  TmaStage* ring = reinterpret_cast<TmaStage*>(s_dyn);
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_dyn + sizeof(TmaStage) * kRing);
+  uint64_t* empty = full + kRing;
+  uint32_t* s_tile = reinterpret_cast<uint32_t*>(empty + kRing);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&full[i], 1 + kScaleLanes);  // the producer's expect_tx + one per scale lane
+      mbar_init(&empty[i], kCons);         // one per consumer warp
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == kCons) {
+    strip_producer(groups, ngroups, a, ring, full, empty, lane);
+    return;
+  }
+  constexpr int kCT = 32 * kCons;  // consumer threads
   const Hp h = make_hp(a.hp);
-  StageBuf* st = pipe + warp * kStages;
+  uint32_t k = 0;      // stages consumed
+  bool dead = false;   // a wait timed out: skip the remaining work, keep the barriers
   for (int gi = ngroups - 1 - int(blockIdx.x); gi >= 0; gi -= int(gridDim.x)) {
     const RegionGroup g = groups[gi];
-    // strip: rows x 256 columns, block = one row segment; band: rows x C,
-    // flat 256-element blocks from the band start
     const bool flat = g.width == g.C;
     const int ntile = (g.width + 127) >> 7;
-    if (FP8) {
-      for (int t = threadIdx.x; t < ntile; t += kThreads) s_tile[t] = 0u;
-      __syncthreads();
-    }
     const int nel = g.rows * g.width;
-    const int nblk = flat ? (nel + 255) >> 8 : g.rows;
-    const int rstep = g.C >> 8;  // strip: slots per row
-    // geometry of this warp's k-th block: lane position, valid count, slot
-    auto geom = [&](int k, int64_t& pos, int& n, int& slot) {
-      const int b = warp + k * kWarps;
-      const int off = flat ? (b << 8) : b * g.C;
-      slot = g.mslot + (flat ? b : b * rstep);
-      n = flat ? max(0, min(8, nel - off - lane * 8)) : 8;
-      pos = g.pos + off + lane * 8;
-    };
-    const int nb_w = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
-#pragma unroll
-    for (int k = 0; k < kStages - 1; ++k) {
-      if (k < nb_w) {
-        int64_t pos; int n, slot;
-        geom(k, pos, n, slot);
-        if (n == 8) stage_issue(st[k], lane, a, pos);
-        stage_scales(st[k], lane, a, slot);
-      }
-      cp_async_commit();
+    const int nblk = region_blocks(g);
+    if (FP8) {
+      for (int t = threadIdx.x; t < ntile; t += kCT) s_tile[t] = 0u;
+      consumer_sync();
     }
-    for (int k = 0; k < nb_w; ++k) {
-      const int kn = k + kStages - 1;
-      __syncwarp();
-      if (kn < nb_w) {
-        int64_t pos; int n, slot;
-        geom(kn, pos, n, slot);
-        if (n == 8) stage_issue(st[kn % kStages], lane, a, pos);
-        stage_scales(st[kn % kStages], lane, a, slot);
+    for (int j = 0; j < nblk; j += kCons, ++k) {
+      const int s = int(k % kRing);
+      if (!dead && !__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (k / kRing) & 1))) {
+        dead = true;
+        if (lane == 0) report(a.status, 3);
       }
-      cp_async_commit();
-      cp_async_wait<kStages - 1>();
-      __syncwarp();  // lanes 0 and 1 staged the scales every lane reads
-      int64_t pos; int n, slot;
-      geom(k, pos, n, slot);
-      const StageBuf& sb = st[k % kStages];
-      const Raw8 x = n == 8 ? raw_from_stage(sb, lane) : raw_from_global(a, pos, n);
+      if (dead) continue;
+      const TmaStage& S = ring[s];
+      const int b = j + warp;
+      if (b >= nblk) {
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
+      }
+      int64_t start;
+      int nb, slot;
+      region_block(g, b, start, nb, slot);
+      const bool staged = block_staged(start, nb);
+      const int64_t pos = start + lane * 8;
+      const int n = max(0, min(8, nb - lane * 8));
+      Raw8 x;
+      if (staged) {
+        x.g = S.g[warp][lane];
+        x.p0 = S.p[warp][2 * lane];
+        x.p1 = S.p[warp][2 * lane + 1];
+        x.m = S.m[warp][lane];
+        x.v = S.v[warp][lane];
+      } else {
+        x = raw_from_global(a, pos, n);
+      }
+      const float sm = S.sc[2 * warp], sv = S.sc[2 * warp + 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp no longer reads the stage
       Lane8 o;
-      if (n == 8) adam_raw<true>(h, x, n, sb.sc[0], sb.sc[1], o);
-      else adam_raw<false>(h, x, n, sb.sc[0], sb.sc[1], o);
+      if (staged) adam_raw<true>(h, x, 8, sm, sv, o);
+      else adam_raw<false>(h, x, n, sm, sv, o);
       QScale qm, qv;
       warp_block_scales(o.am, o.av, lane, qm, qv);
       store_state(a, pos, n, o, qm, qv);
@@ -557,7 +695,6 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_strip(const RegionGroup
       if (FP8) {
         if (flat) {
           // column of the lane's first element; several lanes share a tile
-          const int b = warp + k * kWarps;
           const uint32_t e = uint32_t((b << 8) + lane * 8);
           const int col = int(e - fastdiv(e, g.cmul, g.cshr) * uint32_t(g.C));
           const int t = col >> 7;
@@ -566,32 +703,31 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_strip(const RegionGroup
           if (lane == __ffs(same) - 1) atomicMax(&s_tile[t], ap);
         } else {
           // strip: lanes 0-15 cover tile 0, lanes 16-31 tile 1
-          uint32_t ap = o.ap;
-#pragma unroll
-          for (int off = 8; off >= 1; off >>= 1) ap = max(ap, __shfl_xor_sync(0xFFFFFFFFu, ap, off));
+          const uint32_t ap = __reduce_max_sync(lane < 16 ? 0x0000FFFFu : 0xFFFF0000u, o.ap);
           if ((lane & 15) == 0) atomicMax(&s_tile[lane >> 4], ap);
         }
       }
     }
-    cp_async_wait<0>();
     if (FP8) {
-      __syncthreads();
-      for (int t = threadIdx.x; t < ntile; t += kThreads) {
-        const QScale q = qscale(s_tile[t], 448.f);
-        a.fp8_scale[g.fslot + t] = q.s;
-        s_tile[t] = __float_as_uint(q.r);
-        s_tile[ntile + t] = __float_as_uint(q.s);
+      consumer_sync();
+      if (!dead) {
+        for (int t = threadIdx.x; t < ntile; t += kCT) {
+          const QScale q = qscale(s_tile[t], 448.f);
+          a.fp8_scale[g.fslot + t] = q.s;
+          s_tile[t] = __float_as_uint(q.r);
+          s_tile[ntile + t] = __float_as_uint(q.s);
+        }
       }
-      __syncthreads();
-      const int nvec = nel >> 3;
-      constexpr int U = 2;
-      for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * U) {
+      consumer_sync();
+      const int nvec = dead ? 0 : nel >> 3;
+      constexpr int U = 1;
+      for (int v0 = threadIdx.x; v0 < nvec; v0 += kCT * U) {
         float4 p0[U], p1[U];
         int64_t pos[U];
         int tile[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          const int v = v0 + u * kThreads;
+          const int v = v0 + u * kCT;
           if (v < nvec) {
             if (flat) {
               const uint32_t e = uint32_t(v) << 3;
@@ -608,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_strip(const RegionGroup
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          const int v = v0 + u * kThreads;
+          const int v = v0 + u * kCT;
           if (v < nvec) {
             QScale q;
             q.r = __uint_as_float(s_tile[tile[u]]);
@@ -619,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_strip(const RegionGroup
           }
         }
       }
-      __syncthreads();  // s_tile is reused by the next region
+      consumer_sync();  // s_tile is reused by the next region
     }
   }
 }
@@ -783,7 +919,7 @@ int check_launch(const char* what) {
   return BQ_OK;
 }
 
-constexpr int kStripCtasPerSm = kAdamCtas;
+constexpr int kQuantCtasPerSm = kAdamCtas;
 constexpr int kTileCtasPerSm = kAdamCtas;
 constexpr int kMaxStripTiles = 6144;  // 2 words per tile: 48 KB of shared memory
 
@@ -813,8 +949,9 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
     if (int rc = check_launch("bq_step_adam8 (flat128)")) return rc;
   }
   if (t.n_strips) {
-    const int grid = std::min(t.n_strips, sms * kStripCtasPerSm);
-    const size_t smem = sizeof(StageBuf) * kWarps * kStages + 2 * size_t(t.max_strip_tiles) * sizeof(uint32_t);
+    const int grid = std::min(t.n_strips, sms * kStripCtas);
+    const size_t smem = sizeof(TmaStage) * kRing + 2 * kRing * sizeof(uint64_t) +
+                        2 * size_t(t.max_strip_tiles) * sizeof(uint32_t);
     static bool attr_done = false;
     if (!attr_done) {
       cudaFuncSetAttribute(k_strip<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -822,9 +959,9 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
       attr_done = true;
     }
     if (fp8)
-      k_strip<true><<<grid, kThreads, smem, s>>>(t.strips, t.n_strips, a);
+      k_strip<true><<<grid, kStripThreads, smem, s>>>(t.strips, t.n_strips, a);
     else
-      k_strip<false><<<grid, kThreads, smem, s>>>(t.strips, t.n_strips, a);
+      k_strip<false><<<grid, kStripThreads, smem, s>>>(t.strips, t.n_strips, a);
     if (int rc = check_launch("bq_step_adam8 (strips)")) return rc;
   }
   if (t.n_tiles) {
@@ -852,7 +989,7 @@ int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, floa
   }
   if (t.n_strips) {
     const size_t smem = 2 * size_t(std::max(t.max_strip_tiles, 1)) * sizeof(uint32_t);
-    k_quant_region<<<std::min(t.n_strips, sms * kStripCtasPerSm), kThreads, smem, s>>>(t.strips, t.n_strips, master,
+    k_quant_region<<<std::min(t.n_strips, sms * kQuantCtasPerSm), kThreads, smem, s>>>(t.strips, t.n_strips, master,
                                                                                         fp8, fp8_scale);
     if (int rc = check_launch("bq_quant_fp8 (strips)")) return rc;
   }

@@ -144,6 +144,14 @@ int bq_layout_upload(const bq_layout* layout, int dev_lo, int dev_hi, void* dev_
                      bq_stream_t stream, bq_shard** out);
 void bq_shard_free(bq_shard* shard);
 
+/* bq_shard_check - synchronise `stream` and read the shard's device error word
+ * (kept in its workspace): the 2-D Adam kernel's producer / consumer waits give
+ * up after about a second, record where (1, 2: the copy producer; 3: a compute
+ * warp) and let the kernel exit.  BQ_OK if no wait timed out since the last
+ * check (the word is then cleared), BQ_ECUDA otherwise or on a CUDA error.
+ * Defined by no passage of the pages: a failure-reporting aid of this library. */
+int bq_shard_check(const bq_shard* shard, bq_stream_t stream);
+
 /* ------------------------------------------------------------------ step
  * bq_pack - group-level fused pre-communication add / scale / zero / copy.
  * Defined by: DBuffer's fused pre-communication ops (bud-325 summary, Key claims

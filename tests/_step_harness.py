@@ -92,6 +92,7 @@ class StepCase:
         q2 = d(self.fp8_0)
         s2 = d(self.fs0)
         bq.quant_fp8(shard, master, q2, s2, stream=s)
+        bq.shard_check(shard, stream=s)  # no bounded device wait gave up
         torch.cuda.synchronize(dev)
         h = lambda t: None if t is None else t.cpu().numpy()  # noqa: E731
         out = dict(dbuf=h(dbuf).view(np.uint16), master=h(master), m=h(m), v=h(v), ms=h(ms), vs=h(vs),
