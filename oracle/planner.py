@@ -48,6 +48,9 @@ import numpy as np
 # definition, to the library's own; see the export docstring).
 ADAM_FLAT256 = 0
 ADAM_TILE128 = 1
+# a 2-D tensor updated by Muon (momentum, Newton-Schulz at a root, apply): no
+# Adam blocks or scale slots, no FP8 staging
+OPT_MUON = 2
 EXPORT_MAGIC = 0x4251
 EXPORT_VERSION = 1
 
@@ -251,6 +254,9 @@ def _validate(d):
     elif d.adam_kind == ADAM_TILE128:
         if d.g % d.tile_unit():
             raise ValueError("128x128 Adam tiles need g to be whole 128-row bands")
+    elif d.adam_kind == OPT_MUON:
+        if d.rows < 2 or d.fp8:
+            raise ValueError("Muon tensors are 2-D and take no FP8 staging")
     else:
         raise ValueError("unknown Adam block kind")
     if d.fp8 and d.g % d.tile_unit():
@@ -267,6 +273,8 @@ def tiles_in(d, length):
 
 
 def adam_blocks_in(d, length):
+    if d.adam_kind == OPT_MUON:
+        return 0
     if d.adam_kind == ADAM_FLAT256:
         return -(-length // 256)
     return tiles_in(d, length)
@@ -359,7 +367,7 @@ def _blocks(layout, dev_lo, dev_hi, fp8):
     base = layout.dev_table[dev_lo][2 if fp8 else 1]
     for (k, i, t_off, ln, loff, mslot, fslot) in layout.intervals[first:last]:
         d = layout.descs[i]
-        if fp8 and not d.fp8:
+        if (fp8 and not d.fp8) or (not fp8 and d.adam_kind == OPT_MUON):
             continue
         slot = (fslot if fp8 else mslot) - base
         pos0 = (k - dev_lo) * S + loff - t_off  # local position of tensor element 0
@@ -396,7 +404,7 @@ def block_at(layout, dev_lo, dev_hi, pos, fp8=False):
         if not (loff <= loff_in < loff + ln):
             continue
         d = layout.descs[i]
-        if fp8 and not d.fp8:
+        if (fp8 and not d.fp8) or (not fp8 and d.adam_kind == OPT_MUON):
             return None
         slot0 = (fslot if fp8 else mslot) - base
         pos0 = (k - dev_lo) * S + loff - t_off
