@@ -283,6 +283,82 @@ class MuonBatch:
             hy.copy_(y, non_blocking=True)
 
 
+class MuonStep:
+    """The Muon step on the Llama-3-8B layer with its seven matrices on Muon (all
+    8 shards): momentum + gather, Newton-Schulz on the gathered matrices, apply."""
+
+    def __init__(self, dev, seed):
+        import torch
+
+        import block_quant_gb300 as bq
+
+        self.bq, self.torch = bq, torch
+        cfg = W.config("llama3-8b-layer-muon")
+        unit = cfg.units[0]
+        self.layout = bq.plan(unit.tensors, cfg.V, cfg.alpha, cfg.start_align)
+        T = W.Table(self.layout.export())
+        n = cfg.V * T.S
+        self.ws = torch.empty(self.layout.upload_bytes(0, cfg.V), dtype=torch.uint8, device=dev)
+        self.shard = self.layout.upload(0, cfg.V, self.ws)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.dbuf = (torch.randn(n, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+        self.mom = torch.randn(n, generator=g, device=dev) * 1e-3
+        self.master = torch.randn(n, generator=g, device=dev) * 0.02
+        muon = [i for i, t in enumerate(unit.tensors) if t.adam_kind == W.OPT_MUON]
+        shapes = [(unit.tensors[i].rows, unit.tensors[i].cols) for i in muon]
+        self.gath = [torch.empty(r, c, dtype=torch.bfloat16, device=dev) for r, c in shapes]
+        self.outs = [torch.empty_like(x) for x in self.gath]
+        gp, up = np.zeros(len(unit.tensors), np.int64), np.zeros(len(unit.tensors), np.int64)
+        for k, i in enumerate(muon):
+            gp[i], up[i] = self.gath[k].data_ptr(), self.outs[k].data_ptr()
+        self.gp, self.up = torch.from_numpy(gp).to(dev), torch.from_numpy(up).to(dev)
+        self.lr = torch.full((len(unit.tensors),), cfg.muon_lr, dtype=torch.float32, device=dev)
+        self.mu = cfg.mu
+        self.mats = [(x, y, r, c) for x, y, (r, c) in zip(self.gath, self.outs, shapes)]
+        self.nsws = torch.empty(bq.muon_ns_workspace(self.mats), dtype=torch.uint8, device=dev)
+        self.elems = sum(r * c for r, c in shapes)
+        self.flops = muon_flops(shapes)
+        self.shapes = shapes
+        roots = bq.muon_roots(self.layout)
+        load = [0] * cfg.V
+        for i in muon:
+            r, c = unit.tensors[i].rows, unit.tensors[i].cols
+            load[roots[i]] += 5 * (4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3)
+        self.root_tflop = [round(x / 1e12, 3) for x in load]
+        self.V = cfg.V
+
+    def run(self, stream, ev=None):
+        bq = self.bq
+        if ev:
+            ev[0].record(stream)
+        bq.muon_momentum(self.shard, self.dbuf, self.mom, self.mu, self.gp, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        bq.muon_ns(self.mats, self.nsws, steps=5, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        bq.muon_apply(self.shard, self.master, self.up, self.lr, stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    def measure(self, stream, steps, warmup):
+        torch = self.torch
+        for _ in range(warmup):
+            self.run(stream)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for k in range(steps):
+            self.run(stream, evs[k])
+        torch.cuda.synchronize()
+        self.bq.shard_check(self.shard, stream=stream)
+        self.bq.muon_ns_check(self.nsws, stream=stream)
+        mom = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+        ns = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        app = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+        return mom, ns, app
+
+
 def cpu_baseline(seconds=12.0):
     """The oracle, as it stands, on a bounded sample of the same workload: whole
     128-row x 256-column strips of the Llama-3-8B layer's 2-D tensors (pack
@@ -416,6 +492,11 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         muon_e2e = e0.elapsed_time(e1) / km
 
+    mstep = None
+    if args.muon_step:
+        ms_obj = MuonStep(dev, seed=3000 + rank)
+        mstep = ms_obj.measure(stream, steps=5, warmup=3)
+        mstep_max = max_over_ranks(list(mstep), world, device=dev)
     ms_step, dbuf_ms_max, muon_ms_max, e2e_max, muon_e2e_max = max_over_ranks(
         [total_ms / args.steps, dbuf_ms, statistics.mean(muon_ms), e2e_ms, muon_e2e or 0.0], world, device=dev)
     if rank == 0:
@@ -458,6 +539,24 @@ def run_ours(args):
                             "e2e": {"value": round(job_throughput(muon.flops, world, muon_e2e_max) / 1e12, 1),
                                     "unit": "TFLOP/s", "h2d_bytes_per_step": muon.h2d,
                                     "d2h_bytes_per_step": muon.d2h, "ms_per_step": round(muon_e2e_max, 3)}}
+        if mstep:
+            mo, ns, ap = mstep_max
+            tf = ms_obj.flops / (ns * 1e-3) / 1e12
+            gb_m = 12 * ms_obj.elems / (mo * 1e-3) / 1e9
+            gb_a = 10 * ms_obj.elems / (ap * 1e-3) / 1e9
+            line["muon_step"] = {
+                "workload": "llama3-8b-layer, its 7 matrices on Muon (V=8, all shards): momentum + gather, "
+                            "Newton-Schulz x 5 on the gathered matrices, apply",
+                "ms": round(mo + ns + ap, 3), "muon_elements": ms_obj.elems,
+                "momentum": {"ms": round(mo, 4), "GB/s": round(gb_m, 1), "frac": round(gb_m / pk["hbm"], 4),
+                             "bytes": 12 * ms_obj.elems},
+                "ns": {"ms": round(ns, 3), "TFLOP/s": round(tf, 1), "frac": round(tf / pk["bf16_sus"], 4),
+                       "flops": ms_obj.flops},
+                "apply": {"ms": round(ap, 4), "GB/s": round(gb_a, 1), "frac": round(gb_a / pk["hbm"], 4),
+                          "bytes": 10 * ms_obj.elems},
+                "root_ns_tflop_per_device": ms_obj.root_tflop,
+                "note": "measured after the timed region; not part of value",
+            }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
@@ -508,6 +607,8 @@ def main():
     ap.add_argument("--muon", dest="muon", action="store_true", default=True)
     ap.add_argument("--no-muon", dest="muon", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--muon-step", dest="muon_step", action="store_true", default=True)
+    ap.add_argument("--no-muon-step", dest="muon_step", action="store_false")
     ap.add_argument("--shards", type=int, default=None,
                     help="process only local shards [0, K) of the DBuffer (smaller case for profiling)")
     args = ap.parse_args()

@@ -18,14 +18,14 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libbq.so")
 
 BQ_OK, BQ_EINVAL, BQ_EINFEASIBLE, BQ_EALIGN, BQ_ECUDA, BQ_ENOSPC, BQ_EDEVICE = 0, -1, -2, -3, -4, -5, -6
-ADAM_FLAT256, ADAM_TILE128 = 0, 1
+ADAM_FLAT256, ADAM_TILE128, OPT_MUON = 0, 1, 2
 
 # every entry point include/bq.h declares
 SYMBOLS = [
     "bq_strerror", "bq_last_error", "bq_version", "bq_plan", "bq_layout_free", "bq_layout_query",
     "bq_layout_export", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_shard_check", "bq_pack",
     "bq_step_adam8", "bq_quant_fp8", "bq_muon_ns_workspace", "bq_muon_ns", "bq_muon_ns_check",
-    "bq_muon_ns_noalloc",
+    "bq_muon_ns_noalloc", "bq_muon_roots", "bq_muon_momentum", "bq_muon_apply",
 ]
 
 
@@ -93,6 +93,9 @@ def load():
                                P, C.c_size_t, P]
     lib.bq_muon_ns_check.argtypes = [P, C.c_size_t, P]
     lib.bq_shard_check.argtypes = [P, P]
+    lib.bq_muon_roots.argtypes = [P, C.POINTER(C.c_int32), C.c_size_t]
+    lib.bq_muon_momentum.argtypes = [P, P, P, C.c_float, P, P]
+    lib.bq_muon_apply.argtypes = [P, P, P, P, P]
     lib.bq_muon_ns_noalloc.argtypes = [C.c_int, C.POINTER(Mat), C.c_int, C.c_float, C.c_float, C.c_float,
                                        C.c_float, P]
     for name in SYMBOLS:
@@ -254,6 +257,28 @@ def muon_ns(mats, ws, ws_bytes=None, steps=5, a=3.4445, b=-4.7750, c=2.0315, eps
         ws_bytes = ws.numel() * ws.element_size()
     _check(load().bq_muon_ns(len(arr), arr, int(steps), float(a), float(b), float(c), float(eps), _ptr(ws),
                              int(ws_bytes), _stream(stream)))
+
+
+def muon_roots(layout):
+    """Root device of every Muon tensor (-1 for the others), int32 array of N."""
+    n = layout.info()["N"]
+    out = np.zeros(n, np.int32)
+    _check(load().bq_muon_roots(layout.handle, out.ctypes.data_as(C.POINTER(C.c_int32)), n))
+    return out
+
+
+def muon_momentum(shard, grad, mom, mu, gather_ptrs, stream=None):
+    """M <- fma(mu, M, G) on the shard's Muon pieces; bf16(M) into the full
+    matrices whose device pointers gather_ptrs (int64 device tensor, N entries,
+    0 = skip) holds."""
+    _check(load().bq_muon_momentum(shard.handle, _ptr(grad), _ptr(mom), float(mu), _ptr(gather_ptrs),
+                                   _stream(stream)))
+
+
+def muon_apply(shard, master, update_ptrs, lr, stream=None):
+    """W <- fma(-lr[i], O_i, W) on the shard's Muon pieces (update_ptrs: int64
+    device tensor of N bf16 matrix pointers, 0 = skip; lr: fp32 device tensor of N)."""
+    _check(load().bq_muon_apply(shard.handle, _ptr(master), _ptr(update_ptrs), _ptr(lr), _stream(stream)))
 
 
 def shard_check(shard, stream=None):

@@ -51,7 +51,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsPlan {
-  size_t off_pieces, off_chunks, off_f256, off_f128, off_strips, off_tiles, off_status, bytes;
+  size_t off_pieces, off_chunks, off_f256, off_f128, off_strips, off_tiles, off_muon, off_status, bytes;
 };
 
 WsPlan ws_plan(const ShardTables& T) {
@@ -69,6 +69,8 @@ WsPlan ws_plan(const ShardTables& T) {
   o = align_up(o + T.strips.size() * sizeof(RegionGroup), 256);
   p.off_tiles = o;
   o = align_up(o + T.tiles.size() * sizeof(RegionGroup), 256);
+  p.off_muon = o;
+  o = align_up(o + T.muon.size() * sizeof(PackPiece), 256);
   p.off_status = o;  // device error word, zeroed by the upload
   o += 256;
   p.bytes = o;
@@ -143,6 +145,7 @@ int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, s
   put(p.off_f128, T.flat128.data(), T.flat128.size() * sizeof(FlatGroup));
   put(p.off_strips, T.strips.data(), T.strips.size() * sizeof(RegionGroup));
   put(p.off_tiles, T.tiles.data(), T.tiles.size() * sizeof(RegionGroup));
+  put(p.off_muon, T.muon.data(), T.muon.size() * sizeof(PackPiece));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(dev_ws, img.data(), p.bytes, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -162,11 +165,13 @@ int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, s
   sh->dev.flat128 = reinterpret_cast<const FlatGroup*>(base + p.off_f128);
   sh->dev.strips = reinterpret_cast<const RegionGroup*>(base + p.off_strips);
   sh->dev.tiles = reinterpret_cast<const RegionGroup*>(base + p.off_tiles);
+  sh->dev.muon = reinterpret_cast<const PackPiece*>(base + p.off_muon);
   sh->dev.nchunks = T.nchunks;
   sh->dev.n_flat256 = int32_t(T.flat256.size());
   sh->dev.n_flat128 = int32_t(T.flat128.size());
   sh->dev.n_strips = int32_t(T.strips.size());
   sh->dev.n_tiles = int32_t(T.tiles.size());
+  sh->dev.n_muon = int32_t(T.muon.size());
   sh->dev.max_strip_tiles = T.max_strip_tiles;
   sh->dev.status = reinterpret_cast<int*>(base + p.off_status);
   *out = sh;
@@ -210,6 +215,23 @@ int bq_quant_fp8(const bq_shard* sh, const float* master, uint8_t* fp8_out, floa
   if (!aligned16(master) || !aligned16(fp8_out) || (reinterpret_cast<uintptr_t>(fp8_scale) & 3))
     return set_error(BQ_EALIGN, "bq_quant_fp8: misaligned buffer");
   return launch_quant_fp8(sh->dev, master, fp8_out, fp8_scale, stream);
+}
+
+int bq_muon_momentum(const bq_shard* sh, const void* grad, float* mom, float mu, void* const* gather_ptrs,
+                     bq_stream_t stream) {
+  if (!sh || !grad || !mom || !gather_ptrs) return set_error(BQ_EINVAL, "bq_muon_momentum: NULL argument");
+  if (!aligned16(grad) || !aligned16(mom) || (reinterpret_cast<uintptr_t>(gather_ptrs) & 7))
+    return set_error(BQ_EALIGN, "bq_muon_momentum: grad and mom 16-byte, gather_ptrs 8-byte aligned");
+  return launch_muon_momentum(sh->dev, static_cast<const uint16_t*>(grad), mom, mu,
+                              reinterpret_cast<uint16_t* const*>(gather_ptrs), stream);
+}
+
+int bq_muon_apply(const bq_shard* sh, float* master, const void* const* update_ptrs, const float* lr,
+                  bq_stream_t stream) {
+  if (!sh || !master || !update_ptrs || !lr) return set_error(BQ_EINVAL, "bq_muon_apply: NULL argument");
+  if (!aligned16(master) || (reinterpret_cast<uintptr_t>(update_ptrs) & 7) || (reinterpret_cast<uintptr_t>(lr) & 3))
+    return set_error(BQ_EALIGN, "bq_muon_apply: master 16-byte, update_ptrs 8-byte, lr 4-byte aligned");
+  return launch_muon_apply(sh->dev, master, reinterpret_cast<const uint16_t* const*>(update_ptrs), lr, stream);
 }
 
 int bq_shard_check(const bq_shard* sh, bq_stream_t stream) {

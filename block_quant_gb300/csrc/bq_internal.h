@@ -98,6 +98,7 @@ struct ShardTables {
   std::vector<FlatGroup> flat128;     // TILE128 Adam on 1-D tensors (128-element tiles)
   std::vector<RegionGroup> strips;    // FLAT256 Adam + 2-D FP8
   std::vector<RegionGroup> tiles;     // TILE128 Adam on 2-D tensors
+  std::vector<PackPiece> muon;        // Muon tensors: dst local, src tensor offset, <= 8192 elements
   int64_t nchunks = 0;
   int32_t max_strip_tiles = 0;        // most FP8 column tiles in one strip group
 };
@@ -114,8 +115,9 @@ struct DevTables {
   const FlatGroup* flat128;
   const RegionGroup* strips;
   const RegionGroup* tiles;
+  const PackPiece* muon;
   int64_t nchunks;
-  int32_t n_flat256, n_flat128, n_strips, n_tiles;
+  int32_t n_flat256, n_flat128, n_strips, n_tiles, n_muon;
   int32_t max_strip_tiles;
   int* status;  // device error word: 0, or the site of a wait that timed out
 };
@@ -137,6 +139,9 @@ int launch_pack(const DevTables& t, const uint16_t* const* grads, uint16_t* dst,
                 int accumulate, void* stream);
 int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream);
 int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, float* fp8_scale, void* stream);
+int launch_muon_momentum(const DevTables& t, const uint16_t* grad, float* mom, float mu, uint16_t* const* gather,
+                         void* stream);
+int launch_muon_apply(const DevTables& t, float* master, const uint16_t* const* upd, const float* lr, void* stream);
 
 // Muon (ns_gemm.cu)
 int muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes);

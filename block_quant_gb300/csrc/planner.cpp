@@ -70,6 +70,7 @@ int64_t tiles_in(const Tensor& t, int64_t len) {
 }
 
 int64_t adam_blocks_in(const Tensor& t, int64_t len) {
+  if (t.adam_kind == BQ_OPT_MUON) return 0;
   return t.adam_kind == BQ_ADAM_FLAT256 ? ceil_div(len, 256) : tiles_in(t, len);
 }
 
@@ -99,8 +100,10 @@ extern "C" int bq_plan(const bq_tensor_desc* desc, int n, int V, const bq_plan_o
     std::string bad;
     if (t.rows < 1 || t.cols < 0 || t.g < 1 || t.cols > kMaxExtent / std::max<int64_t>(t.rows, 1))
       bad = "bad shape or granularity";
-    else if (t.adam_kind != BQ_ADAM_FLAT256 && t.adam_kind != BQ_ADAM_TILE128)
+    else if (t.adam_kind != BQ_ADAM_FLAT256 && t.adam_kind != BQ_ADAM_TILE128 && t.adam_kind != BQ_OPT_MUON)
       bad = "unknown adam_kind";
+    else if (t.adam_kind == BQ_OPT_MUON && (t.rows < 2 || t.fp8))
+      bad = "Muon tensors are 2-D and take no FP8 staging";
     else if (t.adam_kind == BQ_ADAM_FLAT256 && t.g % 256)
       bad = "FLAT256 Adam blocks need g % 256 == 0";
     else if (t.adam_kind == BQ_ADAM_TILE128 && t.g % t.band())
@@ -221,6 +224,37 @@ extern "C" int bq_layout_query(const bq_layout* L, bq_layout_info* info) {
   return BQ_OK;
 }
 
+// Root of every Muon tensor: longest-processing-time greedy on the nominal
+// Newton-Schulz cost 4 m^2 n + 2 m^3 (m, n = smaller, larger dimension) --
+// largest first (ties: lower tensor index), each to the least-loaded device
+// (ties: lower device index).  A reading of the walkthrough's "load-balanced
+// root" (paper section 6.3), which names no rule.
+extern "C" int bq_muon_roots(const bq_layout* L, int32_t* roots, size_t n) {
+  if (!L || !roots) return set_error(BQ_EINVAL, "bq_muon_roots: NULL argument");
+  if (n < L->tensors.size()) return set_error(BQ_ENOSPC, "bq_muon_roots: roots holds fewer than N entries");
+  using u128 = unsigned __int128;
+  std::vector<std::pair<u128, int>> muon;
+  for (size_t i = 0; i < L->tensors.size(); ++i) {
+    roots[i] = -1;
+    const Tensor& t = L->tensors[i];
+    if (t.adam_kind != BQ_OPT_MUON) continue;
+    const u128 m = u128(std::min(t.rows, t.cols)), nn = u128(std::max(t.rows, t.cols));
+    muon.push_back({4 * m * m * nn + 2 * m * m * m, int(i)});
+  }
+  std::sort(muon.begin(), muon.end(), [](const std::pair<u128, int>& a, const std::pair<u128, int>& b) {
+    return a.first != b.first ? a.first > b.first : a.second < b.second;
+  });
+  std::vector<u128> load(size_t(L->V), 0);
+  for (const auto& c : muon) {
+    size_t k = 0;
+    for (size_t j = 1; j < load.size(); ++j)
+      if (load[j] < load[k]) k = j;
+    roots[c.second] = int32_t(k);
+    load[k] += c.first;
+  }
+  return BQ_OK;
+}
+
 extern "C" int bq_layout_export(const bq_layout* L, int64_t* buf, size_t n) {
   bq_layout_info info;
   if (int rc = bq_layout_query(L, &info)) return rc;
@@ -292,6 +326,7 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
   T.flat128.clear();
   T.strips.clear();
   T.tiles.clear();
+  T.muon.clear();
   T.max_strip_tiles = 0;
   constexpr int64_t kFlatGroupElems = 8192;
   for (int64_t k = first; k < last; ++k) {
@@ -300,6 +335,13 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
     const int64_t pos0 = (v.dev - dev_lo) * S + v.local_off;  // local position of element t_off
     const int32_t mslot = int32_t(v.mslot - mbase);
     const int32_t fslot = v.fslot < 0 ? -1 : int32_t(v.fslot - fbase);
+    if (t.adam_kind == BQ_OPT_MUON) {
+      // Muon: momentum and apply pieces of at most kFlatGroupElems elements
+      for (int64_t off = 0; off < v.len; off += kFlatGroupElems)
+        T.muon.push_back(PackPiece{pos0 + off, v.t_off + off, int32_t(std::min(kFlatGroupElems, v.len - off)),
+                                   int32_t(v.tensor)});
+      continue;
+    }
     if (t.adam_kind == BQ_ADAM_FLAT256 && (t.one_d() || !t.fp8)) {
       for (int64_t off = 0; off < v.len; off += kFlatGroupElems) {
         const int64_t n = std::min(kFlatGroupElems, v.len - off);
@@ -390,6 +432,12 @@ std::string validate_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, co
     if (g.mslot < 0 || mend > nm) return "strip Adam slots out of range";
     if (g.fslot < 0 || g.fslot + ceil_div(g.width, 128) > nf) return "strip FP8 slots out of range";
     if (ceil_div(g.width, 128) > T.max_strip_tiles) return "strip tile count above the shared-memory bound";
+  }
+  for (const PackPiece& p : T.muon) {
+    if (p.len <= 0 || p.dst < 0 || p.dst + p.len > total) return "Muon piece outside the shard range";
+    if (p.tensor < 0 || p.tensor >= int32_t(L.tensors.size()) || L.tensors[p.tensor].adam_kind != BQ_OPT_MUON)
+      return "Muon piece of a non-Muon tensor";
+    if (p.src < 0 || p.src + p.len > L.tensors[p.tensor].numel) return "Muon piece reads outside its tensor";
   }
   for (const RegionGroup& g : T.tiles) {
     if (g.rows <= 0 || g.rows > 128 || g.width <= 0 || g.width > 128 || g.width % 8 || g.C % 8 || g.pos % 8 ||

@@ -825,6 +825,90 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
   }
 }
 
+// ---------------------------------------------------------------- Muon momentum and apply
+// Muon around Newton-Schulz (walkthrough of veScale-FSDP, paper section 6.3): the
+// momentum update runs on the local shards, the full momentum matrix is
+// materialised for the root, and the root's result is applied back to the owned
+// ranges.  One CTA per Muon piece (<= 8192 elements of one tensor interval).
+//   k_muon_momentum: M = fma(mu, M, G) in fp32, stored; bf16(M) (nearest even)
+//                    written to the tensor's row-major matrix at its offset
+//   k_muon_apply:    W = fma(-lr_i, O_i, W), O_i the bf16 Newton-Schulz output
+
+__global__ void __launch_bounds__(kThreads) k_muon_momentum(const PackPiece* __restrict__ pieces,
+                                                            const uint16_t* __restrict__ grad, float* __restrict__ mom,
+                                                            float mu, uint16_t* const* __restrict__ gather) {
+  const PackPiece pc = pieces[blockIdx.x];
+  uint16_t* out = gather[pc.tensor];
+  if (!out) return;
+  out += pc.src;
+  const uint16_t* g = grad + pc.dst;
+  float* m = mom + pc.dst;
+  int e0 = 0;
+  if ((pc.dst & 7) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    const int nv = pc.len >> 3;
+    const float2 mu2 = dup(mu);
+    for (int v = threadIdx.x; v < nv; v += kThreads) {
+      const uint4 gw = reinterpret_cast<const uint4*>(g)[v];
+      const float4 a = reinterpret_cast<const float4*>(m)[2 * v], b = reinterpret_cast<const float4*>(m)[2 * v + 1];
+      const uint32_t w[4] = {gw.x, gw.y, gw.z, gw.w};
+      const float mv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      float r[8];
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 gg = make_float2(bf16f(w[j] & 0xFFFFu), bf16f(w[j] >> 16));
+        const float2 y = fma2(mu2, make_float2(mv[2 * j], mv[2 * j + 1]), gg);
+        r[2 * j] = y.x;
+        r[2 * j + 1] = y.y;
+        o[j] = f2bf(y.x) | (f2bf(y.y) << 16);
+      }
+      reinterpret_cast<float4*>(m)[2 * v] = make_float4(r[0], r[1], r[2], r[3]);
+      reinterpret_cast<float4*>(m)[2 * v + 1] = make_float4(r[4], r[5], r[6], r[7]);
+      reinterpret_cast<uint4*>(out)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    e0 = nv << 3;
+  }
+  for (int e = e0 + threadIdx.x; e < pc.len; e += kThreads) {
+    const float y = __fmaf_rn(mu, m[e], bf16f(g[e]));
+    m[e] = y;
+    out[e] = uint16_t(f2bf(y));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_muon_apply(const PackPiece* __restrict__ pieces, float* __restrict__ master,
+                                                         const uint16_t* const* __restrict__ upd,
+                                                         const float* __restrict__ lr) {
+  const PackPiece pc = pieces[blockIdx.x];
+  const uint16_t* o = upd[pc.tensor];
+  if (!o) return;
+  o += pc.src;
+  float* w = master + pc.dst;
+  const float nlr = -lr[pc.tensor];
+  int e0 = 0;
+  if ((pc.dst & 7) == 0 && (reinterpret_cast<uintptr_t>(o) & 15) == 0) {
+    const int nv = pc.len >> 3;
+    const float2 n2 = dup(nlr);
+    for (int v = threadIdx.x; v < nv; v += kThreads) {
+      const uint4 ow = reinterpret_cast<const uint4*>(o)[v];
+      const float4 a = reinterpret_cast<const float4*>(w)[2 * v], b = reinterpret_cast<const float4*>(w)[2 * v + 1];
+      const uint32_t q[4] = {ow.x, ow.y, ow.z, ow.w};
+      const float wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      float r[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 y = fma2(n2, make_float2(bf16f(q[j] & 0xFFFFu), bf16f(q[j] >> 16)),
+                              make_float2(wv[2 * j], wv[2 * j + 1]));
+        r[2 * j] = y.x;
+        r[2 * j + 1] = y.y;
+      }
+      reinterpret_cast<float4*>(w)[2 * v] = make_float4(r[0], r[1], r[2], r[3]);
+      reinterpret_cast<float4*>(w)[2 * v + 1] = make_float4(r[4], r[5], r[6], r[7]);
+    }
+    e0 = nv << 3;
+  }
+  for (int e = e0 + threadIdx.x; e < pc.len; e += kThreads) w[e] = __fmaf_rn(nlr, bf16f(o[e]), w[e]);
+}
+
 // ---------------------------------------------------------------- standalone FP8
 
 __global__ void __launch_bounds__(kThreads) k_quant_flat(const FlatGroup* __restrict__ groups,
@@ -999,6 +1083,19 @@ int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, floa
     if (int rc = check_launch("bq_quant_fp8 (tiles)")) return rc;
   }
   return BQ_OK;
+}
+
+int launch_muon_momentum(const DevTables& t, const uint16_t* grad, float* mom, float mu, uint16_t* const* gather,
+                         void* stream) {
+  if (!t.n_muon) return BQ_OK;
+  k_muon_momentum<<<t.n_muon, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(t.muon, grad, mom, mu, gather);
+  return check_launch("bq_muon_momentum");
+}
+
+int launch_muon_apply(const DevTables& t, float* master, const uint16_t* const* upd, const float* lr, void* stream) {
+  if (!t.n_muon) return BQ_OK;
+  k_muon_apply<<<t.n_muon, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(t.muon, master, upd, lr);
+  return check_launch("bq_muon_apply");
 }
 
 }  // namespace bq

@@ -50,7 +50,8 @@ enum {
 /* Adam block geometry of a tensor. */
 enum {
   BQ_ADAM_FLAT256 = 0, /* 256 consecutive elements (last block may be short) */
-  BQ_ADAM_TILE128 = 1  /* 128x128 tiles of the 2-D view (1-D tensors: 128 elements) */
+  BQ_ADAM_TILE128 = 1, /* 128x128 tiles of the 2-D view (1-D tensors: 128 elements) */
+  BQ_OPT_MUON = 2      /* 2-D tensor updated by Muon (bq_muon_*): no Adam blocks, no FP8 */
 };
 
 /* One RaggedShard tensor: row-major 2-D view rows x cols (1-D: rows = 1), atomic
@@ -217,6 +218,50 @@ int bq_muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float
  * timed out during the last bq_muon_ns on this workspace, BQ_ECUDA otherwise
  * (or on a CUDA error). */
 int bq_muon_ns_check(const void* ws, size_t ws_bytes, bq_stream_t stream);
+
+/* ------------------------------------------------------------------ the Muon step around Newton-Schulz
+ * Defined by: the Muon experiment of the walkthrough (paper section 6.3).  For
+ * every 2-D weight the optimizer takes its gradient, applies the momentum update,
+ * keeps the original placement, picks a load-balanced root where the full matrix
+ * materialises, runs Newton-Schulz there and sends the result back to be applied
+ * to the weight.  The pages give no formula; the readings implemented:
+ *   momentum  M <- fma(mu, M, G), fp32, one rounding (heavy-ball momentum)
+ *   NS input  bf16(M) (nearest even), the whole matrix in row-major order
+ *   apply     W <- fma(-lr, O, W), fp32, O the bf16 Newton-Schulz output
+ * Tensors planned with adam_kind = BQ_OPT_MUON take this path; bq_step_adam8
+ * leaves them untouched.  On one GPU with every shard of the range resident the
+ * root's gather and the send-back are the device-local copies these calls make;
+ * across GPUs they would be exchanges between ranks (not built here). */
+
+/* bq_muon_roots - root device (0..V-1) of every Muon tensor, -1 for the others,
+ * into roots[0..N).  Rule (a reading; the pages name none): longest-processing-
+ * time greedy on the nominal Newton-Schulz step cost 4 m^2 n + 2 m^3 (m, n the
+ * smaller and larger dimension): largest first (ties: lower tensor index), each
+ * to the device with the least cost assigned so far (ties: lower device index).
+ * Host only.  BQ_ENOSPC if n < N. */
+int bq_muon_roots(const bq_layout* layout, int32_t* roots, size_t n);
+
+/* bq_muon_momentum - momentum update of every Muon tensor piece in the shard's
+ * range: grad is the bf16 gradient DBuffer of local shards [dev_lo, dev_hi)
+ * (after pack), mom the fp32 momentum buffer with the same layout (updated in
+ * place; elements of other tensors and padding untouched).  gather_ptrs is a
+ * DEVICE array of N pointers: entry i is the bf16 row-major rows x cols buffer of
+ * Muon tensor i that receives bf16(M) at each owned tensor offset (the root's
+ * Newton-Schulz input), or NULL to skip tensor i; entries of non-Muon tensors are
+ * never read.  Asynchronous on stream.  BQ_EALIGN: grad, mom not 16-byte or
+ * gather_ptrs not 8-byte aligned. */
+int bq_muon_momentum(const bq_shard* shard, const void* grad, float* mom, float mu, void* const* gather_ptrs,
+                     bq_stream_t stream);
+
+/* bq_muon_apply - W <- fma(-lr[i], O_i, W) over every Muon tensor piece in the
+ * shard's range: master is the fp32 master DBuffer of the range (updated in
+ * place), update_ptrs a DEVICE array of N pointers to the bf16 row-major
+ * Newton-Schulz outputs O_i (NULL: skip tensor i), lr a DEVICE array of N fp32
+ * step sizes (any shape factor folded in by the caller).  Asynchronous on
+ * stream.  BQ_EALIGN: master not 16-byte, update_ptrs not 8-byte, lr not 4-byte
+ * aligned. */
+int bq_muon_apply(const bq_shard* shard, float* master, const void* const* update_ptrs, const float* lr,
+                  bq_stream_t stream);
 
 /* bq_muon_ns_noalloc - bq_muon_ns for callers that cannot allocate device memory
  * when the step runs (a runtime that reserves all GPU memory up front and

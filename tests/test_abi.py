@@ -184,3 +184,27 @@ def test_fastdiv_formula():
         ns = [0, 1, d - 1, d, d + 1, (1 << 31) - 1, (1 << 31) - d] + [int(x) for x in rng.integers(0, 1 << 31, 2000)]
         for n in ns:
             assert ((n * m) >> 32) >> (l - 1) == n // d, (n, d)
+
+
+def test_muon_roots_and_layout_match_oracle(built):
+    """Host logic of the Muon path: the library's root assignment and exported
+    layout equal the oracle's on random groups mixing Muon and Adam tensors."""
+    import block_quant_gb300 as bq
+    from oracle import muon as OM
+
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        V = int(rng.integers(1, 7))
+        descs = []
+        for _ in range(int(rng.integers(1, 12))):
+            r, c = (int(x) for x in rng.integers(2, 40, 2) * 8)
+            kind = int(rng.choice([0, 2, 2]))
+            descs.append((r, c, c if kind == 2 else 256 * c, kind, 0))
+        L = bq.plan(descs, V, 128, 16)
+        od = [P.TensorDesc(*d[:4]) for d in descs]
+        assert list(bq.muon_roots(L)) == OM.muon_roots(od, V)
+        assert np.array_equal(L.export(), np.asarray(P.plan(od, V, 128, 16).export(), np.int64))
+    with pytest.raises(bq.BQError):
+        bq.plan([(1, 256, 256, 2, 0)], 2, 128, 16)  # Muon tensors are 2-D
+    with pytest.raises(bq.BQError):
+        bq.plan([(256, 256, 256, 2, 1)], 2, 128, 16)  # and take no FP8

@@ -23,9 +23,10 @@ CHUNK = 1 << 16
 
 ADAM_FLAT256 = 0
 ADAM_TILE128 = 1
+OPT_MUON = 2
 
 # kinds of random stream
-K_MASTER, K_GRAD, K_MCODE, K_VCODE, K_MSCALE, K_VSCALE, K_MUON = range(7)
+K_MASTER, K_GRAD, K_MCODE, K_VCODE, K_MSCALE, K_VSCALE, K_MUON, K_MOM, K_NSOUT = range(9)
 
 
 @dataclass
@@ -66,6 +67,8 @@ class Config:
     eps: float = 1e-8
     t: int = 10
     muon_shapes: list = field(default_factory=list)
+    mu: float = 0.95        # Muon momentum
+    muon_lr: float = 0.02   # Muon step size
 
 
 def _t(name, rows, cols, g_rows_2d, g_1d, adam_kind, fp8):
@@ -140,6 +143,10 @@ def config(name):
     if name == "muon-ns":
         return Config(5, name, V=1, dev_lo=0, dev_hi=1,
                       muon_shapes=[(4096, 4096), (4096, 14336), (14336, 4096)])
+    if name == "llama3-8b-layer-muon":
+        # the Llama-3-8B layer with its seven matrices on Muon, norms on 8-bit Adam
+        ts = _muonise(_llama_layer(4096, 14336, 32, 8, 128, 256, ADAM_FLAT256, True), 128)
+        return Config(6, name, V=8, dev_lo=0, dev_hi=8, units=[Unit("layer", ts)])
     # ---- small variants: same structure, sizes the oracle finishes in seconds
     if name == "toy-small":
         c = config("toy")
@@ -159,11 +166,22 @@ def config(name):
     if name == "muon-small":
         return Config(15, name, V=1, dev_lo=0, dev_hi=1,
                       muon_shapes=[(256, 256), (256, 640), (640, 256), (200, 328)])
+    if name == "muon-step-small":
+        # Muon matrices cut at single rows (intervals end mid-band), ragged sizes
+        ts = _muonise(_llama_layer(512, 1472, 4, 1, 128, 256, ADAM_FLAT256, True), 1)
+        ts.append(TensorSpec("odd", 200, 328, 328, OPT_MUON, False))
+        return Config(16, name, V=8, dev_lo=0, dev_hi=8, units=[Unit("layer", ts)])
     raise KeyError(name)
+
+
+def _muonise(ts, g_rows):
+    """2-D tensors of a list moved to Muon with a granularity of g_rows rows."""
+    return [TensorSpec(t.name, t.rows, t.cols, g_rows * t.cols, OPT_MUON, False) if t.rows > 1 else t for t in ts]
 
 
 NAMED = ["toy", "llama3-8b-layer", "llama3-70b-rank0", "gpt-oss-120b-rank0", "muon-ns"]
 SMALL = ["toy-small", "llama-small", "llama-tile-small", "gptoss-small", "muon-small"]
+MUON_STEP = ["muon-step-small", "llama3-8b-layer-muon"]
 
 
 # ----------------------------------------------------------------------------- generators
@@ -210,6 +228,19 @@ def mcode_values(cfg_id, unit_id, tensor_id, lo, hi):
 def vcode_values(cfg_id, unit_id, tensor_id, lo, hi):
     return _chunked(cfg_id, unit_id, tensor_id, K_VCODE, lo, hi,
                     lambda r, n: r.integers(64, 256, n).astype(np.uint8), np.uint8)
+
+
+def mom_values(cfg_id, unit_id, tensor_id, lo, hi):
+    """Prior Muon momentum: fp32 ~ N(0, 1e-3)."""
+    return _chunked(cfg_id, unit_id, tensor_id, K_MOM, lo, hi,
+                    lambda r, n: r.normal(0.0, 1e-3, n).astype(np.float32), np.float32)
+
+
+def ns_out_bits(cfg_id, tensor_id, n):
+    """A stand-in Newton-Schulz output for testing the apply step alone: bf16
+    bits of N(0, 0.02) (the size of an orthogonalised matrix's entries)."""
+    return _to_bf16_bits(_chunked(cfg_id, 0, tensor_id, K_NSOUT, 0, n,
+                                  lambda r, m: r.normal(0.0, 0.02, m).astype(np.float32), np.float32))
 
 
 def scale_values(cfg_id, unit_id, which, lo, hi):
