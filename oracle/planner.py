@@ -48,6 +48,9 @@ import numpy as np
 # definition, to the library's own; see the export docstring).
 ADAM_FLAT256 = 0
 ADAM_TILE128 = 1
+# 32x32 tiles of the 2-D view (1-D tensors: 32-element blocks): the 8-bit Adam
+# blocks of the pages' own experiment (paper section 6.3), with 32-row granularity
+ADAM_TILE32 = 3
 # a 2-D tensor updated by Muon (momentum, Newton-Schulz at a root, apply): no
 # Adam blocks or scale slots, no FP8 staging
 OPT_MUON = 2
@@ -254,6 +257,9 @@ def _validate(d):
     elif d.adam_kind == ADAM_TILE128:
         if d.g % d.tile_unit():
             raise ValueError("128x128 Adam tiles need g to be whole 128-row bands")
+    elif d.adam_kind == ADAM_TILE32:
+        if d.g % (32 if d.rows == 1 else 32 * d.cols) or d.fp8:
+            raise ValueError("32x32 Adam tiles need g to be whole 32-row bands and take no FP8 staging")
     elif d.adam_kind == OPT_MUON:
         if d.rows < 2 or d.fp8:
             raise ValueError("Muon tensors are 2-D and take no FP8 staging")
@@ -272,9 +278,20 @@ def tiles_in(d, length):
     return -(-rows // 128) * -(-d.cols // 128)
 
 
+def tiles32_in(d, length):
+    """32x32 tiles (1-D: 32-element blocks) covering ``length`` elements of d that
+    start on a 32-row band boundary."""
+    if d.rows == 1:
+        return -(-length // 32)
+    rows = length // d.cols
+    return -(-rows // 32) * -(-d.cols // 32)
+
+
 def adam_blocks_in(d, length):
     if d.adam_kind == OPT_MUON:
         return 0
+    if d.adam_kind == ADAM_TILE32:
+        return tiles32_in(d, length)
     if d.adam_kind == ADAM_FLAT256:
         return -(-length // 256)
     return tiles_in(d, length)
@@ -375,6 +392,8 @@ def _blocks(layout, dev_lo, dev_hi, fp8):
             for f in range(t_off, t_off + ln, 256):
                 yield slot, pos0 + range_array(f, min(f + 256, t_off + ln))
                 slot += 1
+        elif not fp8 and d.adam_kind == ADAM_TILE32:
+            yield from _tiles(d, t_off, ln, pos0, slot, 32)
         elif d.rows == 1:
             for f in range(t_off, t_off + ln, 128):
                 yield slot, pos0 + range_array(f, min(f + 128, t_off + ln))
@@ -388,6 +407,24 @@ def _blocks(layout, dev_lo, dev_hi, fp8):
                     cols = range_array(cb, min(cb + 128, C))
                     yield slot, pos0 + (rows[:, None] * C + cols[None, :]).ravel()
                     slot += 1
+
+
+def _tiles(d, t_off, ln, pos0, slot, T):
+    """T x T tiles (1-D: T-element blocks) of the interval, band-major,
+    column-tile-minor, clipped at the tensor's edges."""
+    if d.rows == 1:
+        for f in range(t_off, t_off + ln, T):
+            yield slot, pos0 + range_array(f, min(f + T, t_off + ln))
+            slot += 1
+        return
+    C = d.cols
+    r0, r1 = t_off // C, (t_off + ln) // C
+    for rb in range(r0, r1, T):
+        rows = range_array(rb, min(rb + T, r1))
+        for cb in range(0, C, T):
+            cols = range_array(cb, min(cb + T, C))
+            yield slot, pos0 + (rows[:, None] * C + cols[None, :]).ravel()
+            slot += 1
 
 
 def block_at(layout, dev_lo, dev_hi, pos, fp8=False):
@@ -413,17 +450,18 @@ def block_at(layout, dev_lo, dev_hi, pos, fp8=False):
             j = (f - t_off) // 256
             a = t_off + 256 * j
             return slot0 + j, pos0 + range_array(a, min(a + 256, t_off + ln))
+        T = 32 if (not fp8 and d.adam_kind == ADAM_TILE32) else 128
         if d.rows == 1:
-            j = (f - t_off) // 128
-            a = t_off + 128 * j
-            return slot0 + j, pos0 + range_array(a, min(a + 128, t_off + ln))
+            j = (f - t_off) // T
+            a = t_off + T * j
+            return slot0 + j, pos0 + range_array(a, min(a + T, t_off + ln))
         C = d.cols
         r0, r1 = t_off // C, (t_off + ln) // C
         r, c = f // C, f % C
-        band, ct = (r - r0) // 128, c // 128
-        nct = -(-C // 128)
-        rows = range_array(r0 + 128 * band, min(r0 + 128 * band + 128, r1))
-        cols = range_array(128 * ct, min(128 * ct + 128, C))
+        band, ct = (r - r0) // T, c // T
+        nct = -(-C // T)
+        rows = range_array(r0 + T * band, min(r0 + T * band + T, r1))
+        cols = range_array(T * ct, min(T * ct + T, C))
         return slot0 + band * nct + ct, pos0 + (rows[:, None] * C + cols[None, :]).ravel()
     return None
 

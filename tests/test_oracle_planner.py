@@ -99,7 +99,7 @@ def _all_units(names):
             yield name, c, u
 
 
-@pytest.mark.parametrize("name", W.NAMED[:4] + W.SMALL[:4])
+@pytest.mark.parametrize("name", W.NAMED[:4] + W.SMALL[:4] + W.TILE32 + W.MUON_STEP)
 def test_config_layouts_invariants_and_locality(name):
     c = W.config(name)
     for u in c.units:
@@ -139,8 +139,8 @@ def test_config_layouts_invariants_and_locality(name):
                 assert len(slots) == (L.n_fslots if fp8 else L.n_mslots)
                 want = np.zeros_like(seen)
                 for i, dd in enumerate(d):
-                    if fp8 and not dd.fp8:
-                        continue
+                    if (fp8 and not dd.fp8) or (not fp8 and dd.adam_kind == P.OPT_MUON):
+                        continue  # Muon tensors have no Adam blocks
                     want[L.starts[i]:L.starts[i] + dd.numel] = 1
                 assert np.array_equal(seen, want)
 
@@ -152,6 +152,24 @@ def test_tile_shapes_clip_at_edges():
     # 300 rows = 128 + 128 + 44, 200 cols = 128 + 72
     want = sorted([128 * 128, 128 * 72] * 2 + [44 * 128, 44 * 72])
     assert shapes == want
+
+
+def test_tile32_shapes_clip_at_edges():
+    """32x32 blocks of a 70 x 40 tensor: rows 32 + 32 + 6, columns 32 + 8, in
+    band-major, column-minor slot order; a 1-D tensor: 32-element blocks."""
+    d = [P.TensorDesc(70, 40, 32 * 40, P.ADAM_TILE32), P.TensorDesc(1, 100, 32, P.ADAM_TILE32)]
+    L = P.plan(d, 2, 16, 16)
+    blocks = list(P.adam_blocks(L, 0, 2))
+    assert [len(pos) for _, pos in blocks] == [32 * 32, 32 * 8, 32 * 32, 32 * 8, 6 * 32, 6 * 8, 32, 32, 32, 4]
+    assert [slot for slot, _ in blocks] == list(range(10))
+    # the second tile of the first band: rows 0..31, columns 32..39
+    _, pos = blocks[1]
+    want = L.starts[0] + (np.arange(32)[:, None] * 40 + np.arange(32, 40)[None, :]).ravel()
+    assert np.array_equal(np.sort(pos), np.sort(want))
+    with pytest.raises(ValueError):
+        P.plan([P.TensorDesc(64, 40, 16 * 40, P.ADAM_TILE32)], 2, 16, 16)  # 16-row granularity
+    with pytest.raises(ValueError):
+        P.plan([P.TensorDesc(64, 40, 32 * 40, P.ADAM_TILE32, True)], 2, 16, 16)  # no FP8
 
 
 def test_export_format_roundtrip():
@@ -195,7 +213,8 @@ def test_golden_layouts_unchanged():
             (w["S"], w["NI"], w["n_mslots"], w["n_fslots"], w["starts"]), key
 
 
-@pytest.mark.parametrize("name,dev", [("gptoss-small", (0, 8)), ("llama-tile-small", (1, 3)), ("toy", (2, 4))])
+@pytest.mark.parametrize("name,dev", [("gptoss-small", (0, 8)), ("llama-tile-small", (1, 3)), ("toy", (2, 4)),
+                                      ("llama-tile32-small", (2, 6)), ("muon-step-small", (0, 8))])
 def test_block_at_agrees_with_enumeration(name, dev):
     """block_at (used to sample full-size outputs) finds the same slot and
     positions as the full enumeration, for every block and tile."""

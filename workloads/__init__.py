@@ -24,6 +24,7 @@ CHUNK = 1 << 16
 ADAM_FLAT256 = 0
 ADAM_TILE128 = 1
 OPT_MUON = 2
+ADAM_TILE32 = 3
 
 # kinds of random stream
 K_MASTER, K_GRAD, K_MCODE, K_VCODE, K_MSCALE, K_VSCALE, K_MUON, K_MOM, K_NSOUT = range(9)
@@ -147,6 +148,10 @@ def config(name):
         # the Llama-3-8B layer with its seven matrices on Muon, norms on 8-bit Adam
         ts = _muonise(_llama_layer(4096, 14336, 32, 8, 128, 256, ADAM_FLAT256, True), 128)
         return Config(6, name, V=8, dev_lo=0, dev_hi=8, units=[Unit("layer", ts)])
+    if name == "llama3-8b-layer-tile32":
+        # the pages' own 8-bit Adam geometry: 32x32 blocks, 32-row granularity, no FP8
+        ts = _llama_layer(4096, 14336, 32, 8, 128, 256, ADAM_TILE32, False, g_rows=32)
+        return Config(7, name, V=8, dev_lo=0, dev_hi=8, units=[Unit("layer", ts)])
     # ---- small variants: same structure, sizes the oracle finishes in seconds
     if name == "toy-small":
         c = config("toy")
@@ -166,6 +171,11 @@ def config(name):
     if name == "muon-small":
         return Config(15, name, V=1, dev_lo=0, dev_hi=1,
                       muon_shapes=[(256, 256), (256, 640), (640, 256), (200, 328)])
+    if name == "llama-tile32-small":
+        # 32x32 blocks: ragged row bands (1464 rows) and a ragged column tile (328 cols)
+        ts = _llama_layer(512, 1464, 4, 1, 128, 32, ADAM_TILE32, False, g_rows=32)
+        ts.append(TensorSpec("odd", 200, 328, 32 * 328, ADAM_TILE32, False))
+        return Config(17, name, V=8, dev_lo=0, dev_hi=8, units=[Unit("layer", ts)])
     if name == "muon-step-small":
         # Muon matrices cut at single rows (intervals end mid-band), ragged sizes
         ts = _muonise(_llama_layer(512, 1472, 4, 1, 128, 256, ADAM_FLAT256, True), 1)
@@ -182,6 +192,7 @@ def _muonise(ts, g_rows):
 NAMED = ["toy", "llama3-8b-layer", "llama3-70b-rank0", "gpt-oss-120b-rank0", "muon-ns"]
 SMALL = ["toy-small", "llama-small", "llama-tile-small", "gptoss-small", "muon-small"]
 MUON_STEP = ["muon-step-small", "llama3-8b-layer-muon"]
+TILE32 = ["llama-tile32-small", "llama3-8b-layer-tile32"]
 
 
 # ----------------------------------------------------------------------------- generators
