@@ -80,12 +80,14 @@ def step_bytes(table, dev_lo, dev_hi):
     pads = total - elems
     m0, m1 = table.slot_range(dev_lo, dev_hi)
     f0, f1 = table.slot_range(dev_lo, dev_hi, fp8=True)
-    fp8_elems = 0
+    fp8_elems = adam_elems = 0
     for k, i, t_off, ln, loff, ms, fs in iv:
         if fs >= 0:
             fp8_elems += int(ln)
+        if table.tensors[i][5] != W.OPT_MUON:  # Muon tensors are not touched by the Adam step
+            adam_elems += int(ln)
     pack = 4 * elems + 2 * pads
-    adam = 14 * elems + fp8_elems + 16 * (m1 - m0) + 4 * (f1 - f0)
+    adam = 14 * adam_elems + fp8_elems + 16 * (m1 - m0) + 4 * (f1 - f0)
     return dict(elems=elems, pads=pads, pack=pack, adam=adam, total=pack + adam,
                 adam_blocks=m1 - m0, fp8_tiles=f1 - f0)
 
@@ -95,7 +97,11 @@ def adam_launches(table, dev_lo, dev_hi):
     kinds = set()
     for k, i, t_off, ln, loff, ms, fs in table.dev_intervals(dev_lo, dev_hi):
         _, _, rows, cols, g, kind, fp8 = table.tensors[i]
-        if kind == W.ADAM_FLAT256 and (rows == 1 or not fp8):
+        if kind == W.OPT_MUON:
+            continue
+        if kind == W.ADAM_TILE32:
+            kinds.add("flat32" if rows == 1 else "tile32")
+        elif kind == W.ADAM_FLAT256 and (rows == 1 or not fp8):
             kinds.add("flat256")
         elif kind == W.ADAM_TILE128 and rows == 1:
             kinds.add("flat128")
@@ -281,6 +287,27 @@ class MuonBatch:
         self.run(stream)
         for y, hy in zip(self.ys, self.hy):
             hy.copy_(y, non_blocking=True)
+
+
+def time_dbuffer(step, stream, steps, warmup):
+    """Mean pack and Adam milliseconds of a DBufferStep (CUDA events)."""
+    import torch
+
+    for _ in range(warmup):
+        step.pack(stream)
+        step.adam(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e in evs:
+        e[0].record(stream)
+        step.pack(stream)
+        e[1].record(stream)
+        step.adam(stream)
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    step.bq.shard_check(step.shard, stream=stream)
+    return (statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+            statistics.mean(e[1].elapsed_time(e[2]) for e in evs))
 
 
 class MuonStep:
@@ -492,6 +519,13 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         muon_e2e = e0.elapsed_time(e1) / km
 
+    t32 = None
+    if args.tile32:
+        st32 = DBufferStep(W.config("llama3-8b-layer-tile32"), dev, seed=4000 + rank)
+        t32 = max_over_ranks(list(time_dbuffer(st32, stream, steps=20, warmup=3)), world, device=dev)
+        t32_bytes = st32.bytes
+        del st32
+        torch.cuda.empty_cache()
     mstep = None
     if args.muon_step:
         ms_obj = MuonStep(dev, seed=3000 + rank)
@@ -539,6 +573,17 @@ def run_ours(args):
                             "e2e": {"value": round(job_throughput(muon.flops, world, muon_e2e_max) / 1e12, 1),
                                     "unit": "TFLOP/s", "h2d_bytes_per_step": muon.h2d,
                                     "d2h_bytes_per_step": muon.d2h, "ms_per_step": round(muon_e2e_max, 3)}}
+        if t32:
+            pk_ms, ad_ms = t32
+            gb = t32_bytes["adam"] / (ad_ms * 1e-3) / 1e9
+            line["adam_tile32"] = {
+                "workload": "llama3-8b-layer with the pages' 32x32 8-bit Adam blocks, 32-row granularity, no FP8 "
+                            "(V=8, all shards)",
+                "adam_ms": round(ad_ms, 4), "GB/s": round(gb, 1), "frac": round(gb / pk["hbm"], 4),
+                "bytes": t32_bytes["adam"], "adam_blocks": t32_bytes["adam_blocks"],
+                "step_GB/s": round(t32_bytes["total"] / ((pk_ms + ad_ms) * 1e-3) / 1e9, 1),
+                "note": "measured after the timed region; not part of value",
+            }
         if mstep:
             mo, ns, ap = mstep_max
             tf = ms_obj.flops / (ns * 1e-3) / 1e12
@@ -607,6 +652,8 @@ def main():
     ap.add_argument("--muon", dest="muon", action="store_true", default=True)
     ap.add_argument("--no-muon", dest="muon", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile32", dest="tile32", action="store_true", default=True)
+    ap.add_argument("--no-tile32", dest="tile32", action="store_false")
     ap.add_argument("--muon-step", dest="muon_step", action="store_true", default=True)
     ap.add_argument("--no-muon-step", dest="muon_step", action="store_false")
     ap.add_argument("--shards", type=int, default=None,

@@ -18,7 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libbq.so")
 
 BQ_OK, BQ_EINVAL, BQ_EINFEASIBLE, BQ_EALIGN, BQ_ECUDA, BQ_ENOSPC, BQ_EDEVICE = 0, -1, -2, -3, -4, -5, -6
-ADAM_FLAT256, ADAM_TILE128, OPT_MUON = 0, 1, 2
+ADAM_FLAT256, ADAM_TILE128, OPT_MUON, ADAM_TILE32 = 0, 1, 2, 3
 
 # every entry point include/bq.h declares
 SYMBOLS = [

@@ -99,6 +99,8 @@ struct ShardTables {
   std::vector<RegionGroup> strips;    // FLAT256 Adam + 2-D FP8
   std::vector<RegionGroup> tiles;     // TILE128 Adam on 2-D tensors
   std::vector<PackPiece> muon;        // Muon tensors: dst local, src tensor offset, <= 8192 elements
+  std::vector<FlatGroup> flat32;      // TILE32 Adam on 1-D tensors (32-element blocks)
+  std::vector<RegionGroup> tiles32;   // TILE32 Adam on 2-D tensors: 32-row band x <= 256 columns
   int64_t nchunks = 0;
   int32_t max_strip_tiles = 0;        // most FP8 column tiles in one strip group
 };
@@ -116,8 +118,10 @@ struct DevTables {
   const RegionGroup* strips;
   const RegionGroup* tiles;
   const PackPiece* muon;
+  const FlatGroup* flat32;
+  const RegionGroup* tiles32;
   int64_t nchunks;
-  int32_t n_flat256, n_flat128, n_strips, n_tiles, n_muon;
+  int32_t n_flat256, n_flat128, n_strips, n_tiles, n_muon, n_flat32, n_tiles32;
   int32_t max_strip_tiles;
   int* status;  // device error word: 0, or the site of a wait that timed out
 };

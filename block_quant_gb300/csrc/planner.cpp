@@ -69,8 +69,14 @@ int64_t tiles_in(const Tensor& t, int64_t len) {
   return ceil_div(len / t.cols, 128) * ceil_div(t.cols, 128);
 }
 
+int64_t tiles32_in(const Tensor& t, int64_t len) {
+  if (t.one_d()) return ceil_div(len, 32);
+  return ceil_div(len / t.cols, 32) * ceil_div(t.cols, 32);
+}
+
 int64_t adam_blocks_in(const Tensor& t, int64_t len) {
   if (t.adam_kind == BQ_OPT_MUON) return 0;
+  if (t.adam_kind == BQ_ADAM_TILE32) return tiles32_in(t, len);
   return t.adam_kind == BQ_ADAM_FLAT256 ? ceil_div(len, 256) : tiles_in(t, len);
 }
 
@@ -100,8 +106,13 @@ extern "C" int bq_plan(const bq_tensor_desc* desc, int n, int V, const bq_plan_o
     std::string bad;
     if (t.rows < 1 || t.cols < 0 || t.g < 1 || t.cols > kMaxExtent / std::max<int64_t>(t.rows, 1))
       bad = "bad shape or granularity";
-    else if (t.adam_kind != BQ_ADAM_FLAT256 && t.adam_kind != BQ_ADAM_TILE128 && t.adam_kind != BQ_OPT_MUON)
+    else if (t.adam_kind != BQ_ADAM_FLAT256 && t.adam_kind != BQ_ADAM_TILE128 && t.adam_kind != BQ_OPT_MUON &&
+             t.adam_kind != BQ_ADAM_TILE32)
       bad = "unknown adam_kind";
+    else if (t.adam_kind == BQ_ADAM_TILE32 && (t.fp8 || t.g % (t.one_d() ? 32 : 32 * t.cols)))
+      bad = "32x32 Adam tiles need g to be whole 32-row bands and take no FP8 staging";
+    else if (t.adam_kind == BQ_ADAM_TILE32 && !t.one_d() && (t.cols % 8 || t.cols > (int64_t(1) << 23)))
+      bad = "2-D tensors with 32x32 Adam tiles need cols % 8 == 0 and cols <= 2^23";
     else if (t.adam_kind == BQ_OPT_MUON && (t.rows < 2 || t.fp8))
       bad = "Muon tensors are 2-D and take no FP8 staging";
     else if (t.adam_kind == BQ_ADAM_FLAT256 && t.g % 256)
@@ -327,6 +338,8 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
   T.strips.clear();
   T.tiles.clear();
   T.muon.clear();
+  T.flat32.clear();
+  T.tiles32.clear();
   T.max_strip_tiles = 0;
   constexpr int64_t kFlatGroupElems = 8192;
   for (int64_t k = first; k < last; ++k) {
@@ -340,6 +353,27 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
       for (int64_t off = 0; off < v.len; off += kFlatGroupElems)
         T.muon.push_back(PackPiece{pos0 + off, v.t_off + off, int32_t(std::min(kFlatGroupElems, v.len - off)),
                                    int32_t(v.tensor)});
+      continue;
+    }
+    if (t.adam_kind == BQ_ADAM_TILE32) {
+      if (t.one_d()) {
+        for (int64_t off = 0; off < v.len; off += kFlatGroupElems)
+          T.flat32.push_back(FlatGroup{pos0 + off, int32_t(std::min(kFlatGroupElems, v.len - off)),
+                                       int32_t(mslot + off / 32), -1, 0});
+      } else {
+        // 32-row bands x 256-column chunks: 8 tiles per group, one warp each
+        const int64_t C = t.cols;
+        const int64_t r0 = v.t_off / C, r1 = (v.t_off + v.len) / C;
+        const int64_t nct = ceil_div(C, 32);
+        for (int64_t rb = r0, band = 0; rb < r1; rb += 32, ++band) {
+          const int32_t rows = int32_t(std::min<int64_t>(32, r1 - rb));
+          const int64_t bpos = pos0 + (rb - r0) * C;
+          for (int64_t c0 = 0; c0 < C; c0 += 256)
+            T.tiles32.push_back(RegionGroup{bpos + c0, rows, int32_t(C), int32_t(c0),
+                                            int32_t(std::min<int64_t>(256, C - c0)),
+                                            int32_t(mslot + band * nct + c0 / 32), -1, 0, 0});
+        }
+      }
       continue;
     }
     if (t.adam_kind == BQ_ADAM_FLAT256 && (t.one_d() || !t.fp8)) {
@@ -420,6 +454,14 @@ std::string validate_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, co
   };
   if (!flat_ok(T.flat256, 256)) return "flat 256 group out of range";
   if (!flat_ok(T.flat128, 128)) return "flat 128 group out of range";
+  if (!flat_ok(T.flat32, 32)) return "flat 32 group out of range";
+  for (const RegionGroup& g : T.tiles32) {
+    if (g.rows <= 0 || g.rows > 32 || g.width <= 0 || g.width > 256 || g.width % 8 || g.C % 8 || g.pos % 8 ||
+        g.pos < 0 || g.c0 % 32 || g.c0 + g.width > g.C)
+      return "32x32 tile group shape";
+    if (g.pos + int64_t(g.rows - 1) * g.C + g.width > total) return "32x32 tile group reads outside the shard range";
+    if (g.mslot < 0 || g.mslot + ceil_div(g.width, 32) > nm) return "32x32 tile slots out of range";
+  }
   for (const RegionGroup& g : T.strips) {
     const bool flat = g.width == g.C;
     if (g.rows <= 0 || g.rows > 128 || g.C % 8 || g.width % 8 || g.pos % 8 || g.pos < 0) return "strip shape";

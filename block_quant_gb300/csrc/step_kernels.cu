@@ -825,6 +825,60 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
   }
 }
 
+// ---------------------------------------------------------------- 32x32 Adam tiles
+// The pages' own 8-bit Adam geometry (walkthrough of veScale-FSDP, paper section
+// 6.3): 32x32 blocks of the 2-D view, kept whole on one device by a 32-row
+// granularity.  A group is a 32-row band x <= 256 columns; warp w takes the
+// group's tile w (1..4 eight-element vectors per row).  Phase 1: Adam over the
+// tile, p' written, max|m'| and max v' reduced over the warp.  Phase 2: m' and v'
+// recomputed bit-identically from the untouched old codes (the warp read them
+// moments ago, so the loads hit L1 / L2) and requantised.
+
+__global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGroup* __restrict__ groups, int ngroups,
+                                                              AdamArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Hp h = make_hp(a.hp);
+  for (int gi = ngroups - 1 - int(blockIdx.x); gi >= 0; gi -= int(gridDim.x)) {
+    const RegionGroup g = groups[gi];
+    const int c = warp << 5;
+    if (c >= g.width) continue;  // warp-uniform
+    const int vpr = min(32, g.width - c) >> 3;
+    const int nvec = g.rows * vpr;
+    const int slot = g.mslot + warp;
+    const float sm = a.m_scale[slot], sv = a.v_scale[slot];
+    uint32_t am = 0, av = 0;
+    for (int v = lane; v < nvec; v += 32) {
+      const int r = v / vpr, k = v - r * vpr;
+      const int64_t pos = g.pos + int64_t(r) * g.C + c + (k << 3);
+      const Raw8 x = raw_from_global(a, pos, 8);
+      Lane8 o;
+      adam_raw<true>(h, x, 8, sm, sv, o);
+      store_p8(a.master + pos, o.p1);
+      am = max(am, o.am);
+      av = max(av, o.av);
+    }
+    QScale qm, qv;
+    warp_block_scales(am, av, lane, qm, qv);
+    if (lane == 0) {
+      a.m_scale[slot] = qm.s;
+      a.v_scale[slot] = qv.s;
+    }
+    for (int v = lane; v < nvec; v += 32) {
+      const int r = v / vpr, k = v - r * vpr;
+      const int64_t pos = g.pos + int64_t(r) * g.C + c + (k << 3);
+      Raw8 x;
+      x.g = *reinterpret_cast<const uint4*>(a.grad + pos);
+      x.m = *reinterpret_cast<const uint2*>(a.m + pos);
+      x.v = *reinterpret_cast<const uint2*>(a.v + pos);
+      x.p0 = x.p1 = make_float4(0.f, 0.f, 0.f, 0.f);  // p' is not needed here
+      Lane8 o;
+      adam_raw<true>(h, x, 8, sm, sv, o);
+      *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);
+      *reinterpret_cast<uint2*>(a.v + pos) = codes_uint8(o.v1, qv);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- Muon momentum and apply
 // Muon around Newton-Schulz (walkthrough of veScale-FSDP, paper section 6.3): the
 // momentum update runs on the local shards, the full momentum matrix is
@@ -1031,6 +1085,14 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
   if (t.n_flat128) {
     k_flat<4><<<t.n_flat128, kThreads, 0, s>>>(t.flat128, a);
     if (int rc = check_launch("bq_step_adam8 (flat128)")) return rc;
+  }
+  if (t.n_flat32) {
+    k_flat<1><<<t.n_flat32, kThreads, 0, s>>>(t.flat32, a);
+    if (int rc = check_launch("bq_step_adam8 (flat32)")) return rc;
+  }
+  if (t.n_tiles32) {
+    k_tile32<<<std::min(t.n_tiles32, sms * kAdamCtas), kThreads, 0, s>>>(t.tiles32, t.n_tiles32, a);
+    if (int rc = check_launch("bq_step_adam8 (tiles32)")) return rc;
   }
   if (t.n_strips) {
     const int grid = std::min(t.n_strips, sms * kStripCtas);

@@ -51,7 +51,8 @@ enum {
 enum {
   BQ_ADAM_FLAT256 = 0, /* 256 consecutive elements (last block may be short) */
   BQ_ADAM_TILE128 = 1, /* 128x128 tiles of the 2-D view (1-D tensors: 128 elements) */
-  BQ_OPT_MUON = 2      /* 2-D tensor updated by Muon (bq_muon_*): no Adam blocks, no FP8 */
+  BQ_OPT_MUON = 2,     /* 2-D tensor updated by Muon (bq_muon_*): no Adam blocks, no FP8 */
+  BQ_ADAM_TILE32 = 3   /* 32x32 tiles of the 2-D view (1-D: 32 elements), 32-row granularity, no FP8 */
 };
 
 /* One RaggedShard tensor: row-major 2-D view rows x cols (1-D: rows = 1), atomic

@@ -169,6 +169,9 @@ def sampled_check(case, got, n_blocks=300, n_tiles=24, seed=0):
         assert_bits_equal(f"v scale {slot}", got["vs"][slot:slot + 1], np.array([sv], np.float32))
     if got["fp8"] is None:
         return
+    if case.nf == 0:  # no FP8 tiles in the range: the staging buffer is untouched
+        assert np.all(got["fp8"] == case.fp8_0)
+        return
     done = 0
     for probe in probes(20 * n_tiles):
         if done >= n_tiles:

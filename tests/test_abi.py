@@ -43,7 +43,7 @@ def _descs(unit):
     return [P.TensorDesc(t.rows, t.cols, t.g, t.adam_kind, t.fp8) for t in unit.tensors]
 
 
-@pytest.mark.parametrize("name", W.NAMED[:4] + W.SMALL[1:4])
+@pytest.mark.parametrize("name", W.NAMED[:4] + W.SMALL[1:4] + W.TILE32 + W.MUON_STEP)
 def test_planner_matches_oracle_on_configs(name):
     c = W.config(name)
     for u in c.units:
@@ -155,7 +155,7 @@ def test_shard_tables_pass_host_bounds_check():
     from test_parity_step import _edge_tensors
 
     cases = []
-    for name in W.NAMED[:4] + W.SMALL[:4]:
+    for name in W.NAMED[:4] + W.SMALL[:4] + W.TILE32 + W.MUON_STEP:
         c = W.config(name)
         for u in c.units:
             cases.append((u.tensors, c.V, c.alpha, c.start_align))
@@ -198,8 +198,8 @@ def test_muon_roots_and_layout_match_oracle(built):
         descs = []
         for _ in range(int(rng.integers(1, 12))):
             r, c = (int(x) for x in rng.integers(2, 40, 2) * 8)
-            kind = int(rng.choice([0, 2, 2]))
-            descs.append((r, c, c if kind == 2 else 256 * c, kind, 0))
+            kind = int(rng.choice([0, 2, 2, 3]))
+            descs.append((r, c, {0: 256 * c, 2: c, 3: 32 * c}[kind], kind, 0))
         L = bq.plan(descs, V, 128, 16)
         od = [P.TensorDesc(*d[:4]) for d in descs]
         assert list(bq.muon_roots(L)) == OM.muon_roots(od, V)

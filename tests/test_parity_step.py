@@ -34,6 +34,7 @@ def _compare(case, got, want, fp8=True):
     ("llama-tile-small", None), ("llama-tile-small", (1, 2)),
     ("gptoss-small", None), ("gptoss-small", (2, 7)),
     ("muon-step-small", None), ("muon-step-small", (2, 5)),  # Adam leaves Muon tensors alone
+    ("llama-tile32-small", None), ("llama-tile32-small", (2, 6)),  # 32x32 blocks, ragged bands and columns
 ])
 def test_step_matches_oracle(cuda, name, dev):
     c = W.config(name)
