@@ -190,9 +190,13 @@ class Shard:
         return self._h
 
 
-def plan(descs, V, alpha=128, start_align=16):
+ORDER_GIVEN, ORDER_BLOCK, ORDER_SHAPE = 0, 1, 2
+
+
+def plan(descs, V, alpha=128, start_align=16, order=ORDER_GIVEN):
     """descs: iterable of (rows, cols, g, adam_kind, fp8) or objects with those
-    attributes.  Returns a Layout."""
+    attributes; order: placement order (given / by block size / by shape).
+    Returns a Layout."""
     rows = []
     for d in descs:
         if isinstance(d, (tuple, list)):
@@ -200,7 +204,7 @@ def plan(descs, V, alpha=128, start_align=16):
         else:
             rows.append(TensorDesc(int(d.rows), int(d.cols), int(d.g), int(d.adam_kind), int(bool(d.fp8))))
     arr = (TensorDesc * len(rows))(*rows)
-    opts = PlanOpts(int(alpha), int(start_align), 0, 0)
+    opts = PlanOpts(int(alpha), int(start_align), int(order), 0)
     h = C.c_void_p()
     _check(load().bq_plan(arr, len(rows), int(V), C.byref(opts), C.byref(h)))
     return Layout(h.value)

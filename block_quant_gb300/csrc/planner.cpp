@@ -52,10 +52,10 @@ int64_t earliest_start(int64_t e, int64_t n, int64_t g, int64_t S, int64_t V, in
   }
 }
 
-bool place_all(const std::vector<int64_t>& n, const std::vector<int64_t>& g, int64_t S, int64_t V, int64_t align,
-               std::vector<int64_t>* starts) {
+bool place_all(const std::vector<int64_t>& n, const std::vector<int64_t>& g, const std::vector<int>& ord, int64_t S,
+               int64_t V, int64_t align, std::vector<int64_t>* starts) {
   int64_t end = 0;
-  for (size_t i = 0; i < n.size(); ++i) {
+  for (const int i : ord) {
     const int64_t s = earliest_start(end, n[i], g[i], S, V, align);
     if (s < 0) return false;
     if (starts) (*starts)[i] = s;
@@ -92,7 +92,8 @@ extern "C" int bq_plan(const bq_tensor_desc* desc, int n, int V, const bq_plan_o
   const int64_t alpha = opts ? opts->alpha : 128;
   const int64_t align = opts ? opts->start_align : 16;
   if (alpha < 1 || align < 1) return set_error(BQ_EINVAL, "bq_plan: alpha and start_align must be >= 1");
-  if (opts && opts->order != 0) return set_error(BQ_EINVAL, "bq_plan: only the given tensor order (0) is implemented");
+  const int order_kind = opts ? opts->order : 0;
+  if (order_kind < 0 || order_kind > 2) return set_error(BQ_EINVAL, "bq_plan: order must be 0, 1 or 2");
 
   auto L = new bq_layout();
   L->V = V;
@@ -149,7 +150,20 @@ extern "C" int bq_plan(const bq_tensor_desc* desc, int n, int V, const bq_plan_o
   std::iota(by_size.begin(), by_size.end(), 0);
   std::stable_sort(by_size.begin(), by_size.end(), [&](int a, int b) { return ns[a] > ns[b]; });
 
-  auto feasible = [&](int64_t S) { return place_all(ns, gs, S, V, align, nullptr); };
+  // placement order (walkthrough, paper section 5: default, sorted by block size,
+  // sorted by shape): 0 = as given; 1 = atomic block size g, largest first;
+  // 2 = shape, rows then columns, largest first (equal shapes become neighbours);
+  // ties keep the given order
+  std::vector<int> ord(n);
+  std::iota(ord.begin(), ord.end(), 0);
+  if (order_kind == 1)
+    std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) { return gs[a] > gs[b]; });
+  else if (order_kind == 2)
+    std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) {
+      const Tensor &x = L->tensors[a], &y = L->tensors[b];
+      return x.rows != y.rows ? x.rows > y.rows : x.cols > y.cols;
+    });
+  auto feasible = [&](int64_t S) { return place_all(ns, gs, ord, S, V, align, nullptr); };
   int64_t best = -1, best_k = -1;
   int64_t Lk = alpha;
   for (int k = 0; k <= n; ++k) {
@@ -181,7 +195,7 @@ extern "C" int bq_plan(const bq_tensor_desc* desc, int n, int V, const bq_plan_o
   L->S = best;
   L->case3 = best_k;
   L->start.assign(n, 0);
-  if (best < 0 || !place_all(ns, gs, best, V, align, &L->start)) {
+  if (best < 0 || !place_all(ns, gs, ord, best, V, align, &L->start)) {
     delete L;
     return set_error(BQ_EINFEASIBLE, "bq_plan: no feasible layout");
   }

@@ -66,7 +66,10 @@ typedef struct {
 
 /* Planner options.  alpha: collective alignment of S (elements); start_align:
  * alignment of every tensor start (elements; the step kernels need a multiple of
- * 8); order: 0 = the tensors' given order (the only order implemented). */
+ * 8); order: the tensors' placement order in the buffer (the walkthrough's paper
+ * section 5 names three tried): 0 = as given (the default the pages use), 1 =
+ * atomic block size g, largest first, 2 = shape (rows, then columns), largest
+ * first; ties keep the given order.  BQ_EINVAL for any other value. */
 typedef struct {
   int64_t alpha;
   int64_t start_align;

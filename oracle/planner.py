@@ -114,15 +114,16 @@ def place(ns, gs, order, S, V, start_align):
 # ----------------------------------------------------------------------------- heuristic
 
 
-def plan_sizes(ns, gs, V, alpha, start_align=1):
-    """The prefix / binary-search heuristic.  Returns (S, starts, k_best) where
-    k_best is the length of the winning Case-3 prefix."""
+def plan_sizes(ns, gs, V, alpha, start_align=1, order=None):
+    """The prefix / binary-search heuristic over a fixed placement order (default:
+    the given one).  Returns (S, starts, k_best) where k_best is the length of the
+    winning Case-3 prefix."""
     N = len(ns)
     if N == 0 or V < 1 or alpha < 1 or start_align < 1:
         raise ValueError("empty group or bad V / alignment")
     if any(n < 0 for n in ns) or any(g < 1 for g in gs):
         raise ValueError("bad tensor size or granularity")
-    order = list(range(N))
+    order = list(range(N)) if order is None else list(order)
     total = sum(ns)
     base_cap = roundup(total + N * start_align, alpha)
     by_size = sorted(range(N), key=lambda i: (-ns[i], i))
@@ -354,11 +355,30 @@ class Layout:
         return 1.0 - self.total_elems() / (self.V * self.S)
 
 
-def plan(descs, V, alpha=128, start_align=16):
+ORDER_GIVEN, ORDER_BLOCK, ORDER_SHAPE = 0, 1, 2
+
+
+def placement_order(descs, kind=ORDER_GIVEN):
+    """The orders the walkthrough (paper section 5) says were tried: as given (the
+    default), sorted by block size, sorted by tensor shape.  Readings: block size
+    = atomic granularity g, largest first; shape = (rows, cols), largest first,
+    so equal shapes sit together; ties keep the given order."""
+    idx = list(range(len(descs)))
+    if kind == ORDER_GIVEN:
+        return idx
+    if kind == ORDER_BLOCK:
+        return sorted(idx, key=lambda i: (-descs[i].g, i))
+    if kind == ORDER_SHAPE:
+        return sorted(idx, key=lambda i: (-descs[i].rows, -descs[i].cols, i))
+    raise ValueError("unknown order")
+
+
+def plan(descs, V, alpha=128, start_align=16, order=ORDER_GIVEN):
     """Validate the descriptors, run the heuristic, build the derived tables."""
     for d in descs:
         _validate(d)
-    S, starts, _ = plan_sizes([d.numel for d in descs], [d.g for d in descs], V, alpha, start_align)
+    S, starts, _ = plan_sizes([d.numel for d in descs], [d.g for d in descs], V, alpha, start_align,
+                              placement_order(descs, order))
     return Layout(descs, V, S, starts)
 
 

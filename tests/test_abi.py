@@ -208,3 +208,28 @@ def test_muon_roots_and_layout_match_oracle(built):
         bq.plan([(1, 256, 256, 2, 0)], 2, 128, 16)  # Muon tensors are 2-D
     with pytest.raises(bq.BQError):
         bq.plan([(256, 256, 256, 2, 1)], 2, 128, 16)  # and take no FP8
+
+
+def test_placement_orders_match_oracle(built):
+    """The three placement orders (given, by block size, by shape) give the
+    oracle's layout bit for bit, on the configurations and on random groups."""
+    for name in W.NAMED[:4] + W.SMALL[1:4] + W.TILE32:
+        c = W.config(name)
+        for u in c.units:
+            for order in (bq.ORDER_BLOCK, bq.ORDER_SHAPE):
+                want = np.asarray(P.plan(_descs(u), c.V, c.alpha, c.start_align, order).export(), np.int64)
+                got = bq.plan(u.tensors, c.V, c.alpha, c.start_align, order).export()
+                assert np.array_equal(got, want), (name, u.name, order)
+    rng = np.random.default_rng(29)
+    for _ in range(200):
+        descs = []
+        for _ in range(int(rng.integers(1, 10))):
+            r, cc = int(rng.integers(1, 300)), 8 * int(rng.integers(1, 60))
+            g = 256 if r == 1 else int(np.lcm(256, cc * int(rng.choice([1, 8, 128]))))
+            descs.append(P.TensorDesc(r, cc, g, 0, False))
+        V = int(rng.integers(1, 20))
+        for order in (0, 1, 2):
+            want = np.asarray(P.plan(descs, V, 128, 16, order).export(), np.int64)
+            assert np.array_equal(bq.plan(descs, V, 128, 16, order).export(), want)
+    with pytest.raises(bq.BQError):
+        bq.plan([(1, 256, 256, 0, 0)], 2, order=3)

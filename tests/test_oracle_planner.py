@@ -234,3 +234,21 @@ def test_block_at_agrees_with_enumeration(name, dev):
         covered[pos] = True
     for probe in np.nonzero(~covered)[0][:50]:
         assert P.block_at(L, lo, hi, int(probe)) is None
+
+
+def test_every_placement_order_within_twice_optimum():
+    """The pages' orders (given, by block size, by shape) each keep the prefix
+    heuristic within twice the optimum over all orders and S on tiny inputs; the
+    orders are permutations sorted as stated."""
+    for ns, gs, V, alpha in _tiny_cases(80, 19):
+        descs = [P.TensorDesc(1, n, g) for n, g in zip(ns, gs)]
+        opt = P.brute_force_opt(ns, gs, V, alpha, 1)
+        for kind in (P.ORDER_GIVEN, P.ORDER_BLOCK, P.ORDER_SHAPE):
+            order = P.placement_order(descs, kind)
+            assert sorted(order) == list(range(len(ns)))
+            S, starts, _ = P.plan_sizes(ns, gs, V, alpha, 1, order)
+            P.check_layout(ns, gs, starts, S, V)
+            assert opt <= S <= 2 * opt
+    d = [P.TensorDesc(4, 8, 8), P.TensorDesc(16, 8, 128), P.TensorDesc(4, 8, 32), P.TensorDesc(16, 2, 32)]
+    assert P.placement_order(d, P.ORDER_BLOCK) == [1, 2, 3, 0]
+    assert P.placement_order(d, P.ORDER_SHAPE) == [1, 3, 0, 2]
