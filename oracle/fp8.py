@@ -46,3 +46,27 @@ def quant_fp8(layout, dev_lo, dev_hi, master, fp8_out, fp8_scale, tiles=None):
         fp8_out[pos] = q
         fp8_scale[slot] = s
     return fp8_out, fp8_scale
+
+
+# ----------------------------------------------------------------------------- the view after the AllGather
+# Same sources: the gathered FP8 buffer serves the forward and backward compute,
+# which (DeepSeek-V3 style) reads each parameter as code x tile scale.  Reading
+# (the pages give no formula): the E4M3 code decoded exactly, times the tile's
+# fp32 scale in fp32 (one rounding), then rounded to bf16 (nearest even); only
+# FP8 tensors are written, every other element of the output is left as it was.
+
+def dequant_tile(q, s):
+    """uint8 E4M3 codes and the tile's fp32 scale -> bf16 bits (uint16)."""
+    from .codecs import e4m3_decode, f32_to_bf16_bits
+
+    x = e4m3_decode(np.asarray(q, np.uint8)).astype(np.float32) * F32(s)
+    return f32_to_bf16_bits(x.astype(np.float32))
+
+
+def dequant_fp8(layout, dev_lo, dev_hi, fp8, fp8_scale, out_bf16):
+    """bf16 view of every FP8 tile of local shards [dev_lo, dev_hi); returns an
+    updated copy of out_bf16 (uint16)."""
+    out = np.array(out_bf16, dtype=np.uint16, copy=True)
+    for slot, pos in fp8_tiles(layout, dev_lo, dev_hi):
+        out[pos] = dequant_tile(fp8[pos], fp8_scale[slot])
+    return out

@@ -236,3 +236,45 @@ def test_golden_worked_block():
     assert int(np.float32(sm1).view(np.uint32)) == g["out_sm"]
     q8, s8 = F.fp8_tile(p1[:128])
     assert q8.tolist() == g["fp8_codes"] and int(np.float32(s8).view(np.uint32)) == g["fp8_scale"]
+
+
+def test_dequant_view_pins():
+    """The bf16 view after the AllGather: exact for power-of-two scales (the
+    decoded code times 2^k is exact, then one bf16 rounding of an E4M3 value,
+    which bf16 holds exactly); zero scale gives signed zeros; round trip through
+    the quantiser within E4M3's half-ulp (2^-4 relative for normals) plus bf16's
+    2^-9; only FP8 tiles are written."""
+    from oracle import codecs as OC
+    from oracle import fp8 as OF
+
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]  # the two NaN patterns
+    dec = OC.e4m3_decode(codes).astype(np.float32)
+    for k in (-20, -3, 0, 5):
+        got = OC.bf16_bits_to_f32(OF.dequant_tile(codes, np.float32(2.0 ** k)))
+        assert np.array_equal(got, dec * np.float32(2.0 ** k))
+    z = OC.bf16_bits_to_f32(OF.dequant_tile(codes, np.float32(0)))
+    assert np.all(z == 0) and np.array_equal(np.signbit(z), np.signbit(dec))
+    rng = np.random.default_rng(8)
+    p = rng.normal(0, 0.02, 128 * 128).astype(np.float32)
+    q, s = OF.fp8_tile(p)
+    back = OC.bf16_bits_to_f32(OF.dequant_tile(q, s))
+    amax = np.abs(p).max()
+    normal = np.abs(p) * (448.0 / amax) >= 2.0 ** -6  # scaled value in E4M3's normal range
+    rel = np.abs(back[normal] - p[normal]) / np.abs(p[normal])
+    assert rel.max() <= 2.0 ** -4 + 2.0 ** -8
+    if (~normal).any():  # subnormal codes: half the 2^-9 step, in scaled units
+        assert np.abs(back[~normal] - p[~normal]).max() <= 2.0 ** -10 * s * (1 + 2.0 ** -6) + 2.0 ** -9 * np.abs(p[~normal]).max()
+    # layout level: FP8 tiles written, everything else untouched
+    from oracle import planner as P
+
+    descs = [P.TensorDesc(256, 256, 128 * 256, P.ADAM_FLAT256, True), P.TensorDesc(1, 512, 256, P.ADAM_FLAT256, False)]
+    L = P.plan(descs, 2, 128, 16)
+    n = 2 * L.S
+    master = rng.normal(0, 0.02, n).astype(np.float32)
+    qb, sb = OF.quant_fp8(L, 0, 2, master, np.zeros(n, np.uint8), np.zeros(L.n_fslots, np.float32))
+    out = OF.dequant_fp8(L, 0, 2, qb, sb, np.full(n, 0x7FC1, np.uint16))
+    t0 = L.starts[0]
+    assert np.all(out[:t0] == 0x7FC1) and np.all(out[t0 + 256 * 256:] == 0x7FC1)
+    err = np.abs(OC.bf16_bits_to_f32(out[t0:t0 + 65536]) - master[t0:t0 + 65536])
+    assert err.max() <= 2.0 ** -4 * np.abs(master[t0:t0 + 65536]).max()
