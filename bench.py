@@ -289,6 +289,22 @@ class MuonBatch:
             hy.copy_(y, non_blocking=True)
 
 
+def time_call(fn, stream, steps, warmup):
+    """Mean milliseconds of fn() on stream (CUDA events)."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def time_dbuffer(step, stream, steps, warmup):
     """Mean pack and Adam milliseconds of a DBufferStep (CUDA events)."""
     import torch
@@ -519,6 +535,16 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         muon_e2e = e0.elapsed_time(e1) / km
 
+    dq = None
+    if args.dequant:
+        view = torch.empty(step.n, dtype=torch.bfloat16, device=dev)
+
+        def dq_call():
+            bq.dequant_fp8(step.shard, step.fp8, step.fs, view, stream=stream)
+
+        dq = max_over_ranks([time_call(dq_call, stream, steps=20, warmup=3)], world, device=dev)[0]
+        dq_elems = int(sum(int(r[3]) for r in step.table.dev_intervals(step.lo, step.hi) if r[6] >= 0))
+        del view
     t32 = None
     if args.tile32:
         st32 = DBufferStep(W.config("llama3-8b-layer-tile32"), dev, seed=4000 + rank)
@@ -573,6 +599,14 @@ def run_ours(args):
                             "e2e": {"value": round(job_throughput(muon.flops, world, muon_e2e_max) / 1e12, 1),
                                     "unit": "TFLOP/s", "h2d_bytes_per_step": muon.h2d,
                                     "d2h_bytes_per_step": muon.d2h, "ms_per_step": round(muon_e2e_max, 3)}}
+        if dq:
+            dq_bytes = 3 * dq_elems + 4 * step.bytes["fp8_tiles"]
+            gb = dq_bytes / (dq * 1e-3) / 1e9
+            line["dequant_view"] = {
+                "workload": "llama3-8b-layer FP8 buffer -> bf16 view (code x tile scale), all 8 shards",
+                "ms": round(dq, 4), "GB/s": round(gb, 1), "frac": round(gb / pk["hbm"], 4), "bytes": dq_bytes,
+                "note": "measured after the timed region; not part of value",
+            }
         if t32:
             pk_ms, ad_ms = t32
             gb = t32_bytes["adam"] / (ad_ms * 1e-3) / 1e9
@@ -652,6 +686,8 @@ def main():
     ap.add_argument("--muon", dest="muon", action="store_true", default=True)
     ap.add_argument("--no-muon", dest="muon", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dequant", dest="dequant", action="store_true", default=True)
+    ap.add_argument("--no-dequant", dest="dequant", action="store_false")
     ap.add_argument("--tile32", dest="tile32", action="store_true", default=True)
     ap.add_argument("--no-tile32", dest="tile32", action="store_false")
     ap.add_argument("--muon-step", dest="muon_step", action="store_true", default=True)

@@ -25,7 +25,7 @@ SYMBOLS = [
     "bq_strerror", "bq_last_error", "bq_version", "bq_plan", "bq_layout_free", "bq_layout_query",
     "bq_layout_export", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_shard_check", "bq_pack",
     "bq_step_adam8", "bq_quant_fp8", "bq_muon_ns_workspace", "bq_muon_ns", "bq_muon_ns_check",
-    "bq_muon_ns_noalloc", "bq_muon_roots", "bq_muon_momentum", "bq_muon_apply",
+    "bq_muon_ns_noalloc", "bq_muon_roots", "bq_muon_momentum", "bq_muon_apply", "bq_dequant_fp8",
 ]
 
 
@@ -94,6 +94,7 @@ def load():
     lib.bq_muon_ns_check.argtypes = [P, C.c_size_t, P]
     lib.bq_shard_check.argtypes = [P, P]
     lib.bq_muon_roots.argtypes = [P, C.POINTER(C.c_int32), C.c_size_t]
+    lib.bq_dequant_fp8.argtypes = [P, P, P, P, P]
     lib.bq_muon_momentum.argtypes = [P, P, P, C.c_float, P, P]
     lib.bq_muon_apply.argtypes = [P, P, P, P, P]
     lib.bq_muon_ns_noalloc.argtypes = [C.c_int, C.POINTER(Mat), C.c_int, C.c_float, C.c_float, C.c_float,
@@ -261,6 +262,11 @@ def muon_ns(mats, ws, ws_bytes=None, steps=5, a=3.4445, b=-4.7750, c=2.0315, eps
         ws_bytes = ws.numel() * ws.element_size()
     _check(load().bq_muon_ns(len(arr), arr, int(steps), float(a), float(b), float(c), float(eps), _ptr(ws),
                              int(ws_bytes), _stream(stream)))
+
+
+def dequant_fp8(shard, fp8, fp8_scale, out, stream=None):
+    """bf16 view (code x tile scale) of the FP8 buffer's tiles into out."""
+    _check(load().bq_dequant_fp8(shard.handle, _ptr(fp8), _ptr(fp8_scale), _ptr(out), _stream(stream)))
 
 
 def muon_roots(layout):

@@ -228,6 +228,14 @@ int bq_quant_fp8(const bq_shard* sh, const float* master, uint8_t* fp8_out, floa
   return launch_quant_fp8(sh->dev, master, fp8_out, fp8_scale, stream);
 }
 
+int bq_dequant_fp8(const bq_shard* sh, const uint8_t* fp8, const float* fp8_scale, void* out_bf16, bq_stream_t stream) {
+  if (!sh || !fp8 || !out_bf16) return set_error(BQ_EINVAL, "bq_dequant_fp8: NULL argument");
+  if (!fp8_scale && sh->nf > 0) return set_error(BQ_EINVAL, "bq_dequant_fp8: NULL fp8_scale");
+  if (!aligned16(fp8) || !aligned16(out_bf16) || (reinterpret_cast<uintptr_t>(fp8_scale) & 3))
+    return set_error(BQ_EALIGN, "bq_dequant_fp8: misaligned buffer");
+  return launch_dequant_fp8(sh->dev, fp8, fp8_scale, static_cast<uint16_t*>(out_bf16), stream);
+}
+
 int bq_muon_momentum(const bq_shard* sh, const void* grad, float* mom, float mu, void* const* gather_ptrs,
                      bq_stream_t stream) {
   if (!sh || !grad || !mom || !gather_ptrs) return set_error(BQ_EINVAL, "bq_muon_momentum: NULL argument");

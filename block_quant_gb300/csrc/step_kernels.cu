@@ -1051,6 +1051,74 @@ __global__ void __launch_bounds__(kThreads) k_quant_region(const RegionGroup* __
   }
 }
 
+// ---------------------------------------------------------------- the bf16 view after the AllGather
+// Compute reads each gathered FP8 parameter as code x tile scale: the E4M3 code
+// decoded exactly (every E4M3 value is a half), times the fp32 scale (one fp32
+// rounding), rounded to bf16 (nearest even).  Only FP8 tiles are written.
+
+__device__ __forceinline__ uint4 dequant8(uint2 w, float s) {
+  const uint32_t b[2] = {w.x, w.y};
+  uint32_t o[4];
+  const float2 s2 = dup(s);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_fp8x2_storage_t pair = __nv_fp8x2_storage_t((b[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+    const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3));
+    const float2 x = mul2(__half22float2(h), s2);
+    o[j] = f2bf(x.x) | (f2bf(x.y) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint16_t dequant1(uint8_t c, float s) {
+  const __half h = __half(__nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t(c), __NV_E4M3));
+  return uint16_t(f2bf(__fmul_rn(__half2float(h), s)));
+}
+
+__global__ void __launch_bounds__(kThreads) k_dequant_flat(const FlatGroup* __restrict__ groups,
+                                                           const uint8_t* __restrict__ fp8,
+                                                           const float* __restrict__ fp8_scale,
+                                                           uint16_t* __restrict__ out) {
+  const FlatGroup g = groups[blockIdx.x];
+  if (g.fslot < 0) return;
+  const int nv = g.nelem >> 3;
+  for (int v = threadIdx.x; v < nv; v += kThreads) {
+    const int e = v << 3;  // 8 elements never cross a 128-element tile
+    const int64_t pos = g.pos + e;
+    *reinterpret_cast<uint4*>(out + pos) =
+        dequant8(*reinterpret_cast<const uint2*>(fp8 + pos), fp8_scale[g.fslot + (e >> 7)]);
+  }
+  for (int e = (nv << 3) + threadIdx.x; e < g.nelem; e += kThreads)
+    out[g.pos + e] = dequant1(fp8[g.pos + e], fp8_scale[g.fslot + (e >> 7)]);
+}
+
+__global__ void __launch_bounds__(kThreads) k_dequant_region(const RegionGroup* __restrict__ groups, int ngroups,
+                                                             const uint8_t* __restrict__ fp8,
+                                                             const float* __restrict__ fp8_scale,
+                                                             uint16_t* __restrict__ out) {
+  for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
+    const RegionGroup g = groups[gi];
+    if (g.fslot < 0) continue;
+    const bool flat = g.width == g.C;
+    const int nvec = (g.rows * g.width) >> 3, vpr = g.width >> 3;
+    for (int v = threadIdx.x; v < nvec; v += kThreads) {
+      int64_t pos;
+      int col;
+      if (flat) {
+        const uint32_t e = uint32_t(v) << 3;
+        col = int(e - fastdiv(e, g.cmul, g.cshr) * uint32_t(g.C));
+        pos = g.pos + e;
+      } else {
+        const int r = v / vpr, k = v - r * vpr;
+        col = k << 3;
+        pos = g.pos + int64_t(r) * g.C + col;
+      }
+      *reinterpret_cast<uint4*>(out + pos) =
+          dequant8(*reinterpret_cast<const uint2*>(fp8 + pos), fp8_scale[g.fslot + (col >> 7)]);
+    }
+  }
+}
+
 int check_launch(const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
@@ -1143,6 +1211,28 @@ int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, floa
     k_quant_region<<<std::min(t.n_tiles, sms * kTileCtasPerSm), kThreads, 2 * sizeof(uint32_t), s>>>(
         t.tiles, t.n_tiles, master, fp8, fp8_scale);
     if (int rc = check_launch("bq_quant_fp8 (tiles)")) return rc;
+  }
+  return BQ_OK;
+}
+
+int launch_dequant_fp8(const DevTables& t, const uint8_t* fp8, const float* fp8_scale, uint16_t* out, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = sm_count();
+  if (t.n_flat256) {
+    k_dequant_flat<<<t.n_flat256, kThreads, 0, s>>>(t.flat256, fp8, fp8_scale, out);
+    if (int rc = check_launch("bq_dequant_fp8 (flat256)")) return rc;
+  }
+  if (t.n_flat128) {
+    k_dequant_flat<<<t.n_flat128, kThreads, 0, s>>>(t.flat128, fp8, fp8_scale, out);
+    if (int rc = check_launch("bq_dequant_fp8 (flat128)")) return rc;
+  }
+  if (t.n_strips) {
+    k_dequant_region<<<std::min(t.n_strips, sms * 8), kThreads, 0, s>>>(t.strips, t.n_strips, fp8, fp8_scale, out);
+    if (int rc = check_launch("bq_dequant_fp8 (strips)")) return rc;
+  }
+  if (t.n_tiles) {
+    k_dequant_region<<<std::min(t.n_tiles, sms * 8), kThreads, 0, s>>>(t.tiles, t.n_tiles, fp8, fp8_scale, out);
+    if (int rc = check_launch("bq_dequant_fp8 (tiles)")) return rc;
   }
   return BQ_OK;
 }

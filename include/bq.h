@@ -223,6 +223,19 @@ int bq_muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float
  * (or on a CUDA error). */
 int bq_muon_ns_check(const void* ws, size_t ws_bytes, bq_stream_t stream);
 
+/* bq_dequant_fp8 - the bf16 view of the FP8 buffer after the AllGather.
+ * Defined by: block-wise FP8 training in the DeepSeek-V3 style (bud-325 summary,
+ * TL;DR and Key claims): the gathered E4M3 parameters serve the compute as code
+ * x tile scale.  Reading: each code decoded exactly, times its tile's fp32 scale
+ * in fp32 (one rounding), rounded to bf16 (nearest even).
+ * fp8 / fp8_scale: the staging buffer and tile scales of local shards
+ * [dev_lo, dev_hi) as bq_step_adam8 / bq_quant_fp8 write them; out_bf16: bf16
+ * buffer with the DBuffer layout of the range; only elements of FP8 tiles are
+ * written.  Asynchronous on stream.  BQ_EALIGN: fp8 or out_bf16 not 16-byte
+ * aligned, fp8_scale not 4-byte aligned. */
+int bq_dequant_fp8(const bq_shard* shard, const uint8_t* fp8, const float* fp8_scale, void* out_bf16,
+                   bq_stream_t stream);
+
 /* ------------------------------------------------------------------ the Muon step around Newton-Schulz
  * Defined by: the Muon experiment of the walkthrough (paper section 6.3).  For
  * every 2-D weight the optimizer takes its gradient, applies the momentum update,

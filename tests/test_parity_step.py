@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import block_quant_gb300 as bq
 import workloads as W
 from _step_harness import StepCase, assert_bits_equal
 
@@ -108,3 +109,31 @@ def test_padding_only_devices(cuda):
     got = empty.run_gpu(cuda)
     assert not got["dbuf"].any()
     _compare(empty, got, empty.run_oracle())
+
+
+@pytest.mark.parametrize("name,dev", [("llama-small", None), ("llama-tile-small", (1, 3)), ("gptoss-small", (2, 7)),
+                                      ("toy", None)])
+def test_dequant_view_bit_exact(cuda, name, dev):
+    """bf16 view of the FP8 buffer (code x tile scale) on seeded codes and scales:
+    every FP8 tile bit for bit, every other element untouched."""
+    import torch
+
+    from oracle import fp8 as OF
+
+    c = W.config(name)
+    kw = {} if dev is None else dict(dev_lo=dev[0], dev_hi=dev[1])
+    case = StepCase(c, **kw)
+    rng = np.random.default_rng(31)
+    codes = rng.integers(0, 256, case.n).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] ^= 1  # no NaN patterns
+    scales = (rng.random(max(case.nf, 1)) * 1e-4).astype(np.float32)
+    scales[::7] = 0.0
+    out0 = np.full(case.n, 0x7FC1, np.uint16)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(cuda)  # noqa: E731
+    ws = torch.empty(case.layout.upload_bytes(case.dev_lo, case.dev_hi), dtype=torch.uint8, device=cuda)
+    shard = case.layout.upload(case.dev_lo, case.dev_hi, ws)
+    out = d(out0.view(np.int16))
+    bq.dequant_fp8(shard, d(codes), d(scales), out)
+    torch.cuda.synchronize(cuda)
+    want = OF.dequant_fp8(case.olayout, case.dev_lo, case.dev_hi, codes, scales, out0)
+    assert_bits_equal("bf16 view", out.cpu().numpy().view(np.uint16), want)
