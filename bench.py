@@ -289,6 +289,79 @@ class MuonBatch:
             hy.copy_(y, non_blocking=True)
 
 
+class ModelStep:
+    """The DBuffer step of every unit of a model's rank-0 slice (one DBuffer per
+    unit: embedding, each layer, head), each unit instance with its own buffers;
+    identical units share one upload of the work tables."""
+
+    def __init__(self, name, dev, seed):
+        import torch
+
+        import block_quant_gb300 as bq
+
+        self.bq, self.torch = bq, torch
+        cfg = W.config(name)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.units, self.bytes, self.launches, self.elems = [], 0, 0, 0
+        self.keep = []
+        for u in cfg.units:
+            layout = bq.plan(u.tensors, cfg.V, cfg.alpha, cfg.start_align)
+            T = W.Table(layout.export())
+            lo, hi = cfg.dev_lo, cfg.dev_hi
+            ws = torch.empty(layout.upload_bytes(lo, hi), dtype=torch.uint8, device=dev)
+            shard = layout.upload(lo, hi, ws)
+            self.keep += [layout, ws, shard]
+            b = step_bytes(T, lo, hi)
+            m0, m1 = T.slot_range(lo, hi)
+            f0, f1 = T.slot_range(lo, hi, fp8=True)
+            n = (hi - lo) * T.S
+            for _ in range(u.repeat):
+                grads, ptrs = [], np.zeros(len(u.tensors), np.int64)
+                for i in range(len(u.tensors)):
+                    a, bb = T.owned_range(i, lo, hi)
+                    if bb > a:
+                        gr = (torch.randn(bb - a, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+                        grads.append(gr)
+                        ptrs[i] = gr.data_ptr() - 2 * a
+                unit = dict(
+                    shard=shard, grads=grads, gp=torch.from_numpy(ptrs).to(dev),
+                    dbuf=torch.empty(n, dtype=torch.bfloat16, device=dev),
+                    master=torch.randn(n, generator=g, device=dev) * 0.02,
+                    m=torch.randint(-127, 128, (n,), generator=g, device=dev, dtype=torch.int8),
+                    v=torch.randint(64, 256, (n,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8),
+                    ms=(torch.rand(max(m1 - m0, 1), generator=g, device=dev) + 0.5) * (1e-3 / 127),
+                    vs=(torch.rand(max(m1 - m0, 1), generator=g, device=dev) + 0.5) * (1e-6 / 255),
+                    fp8=torch.zeros(n, dtype=torch.uint8, device=dev),
+                    fs=torch.zeros(max(f1 - f0, 1), dtype=torch.float32, device=dev),
+                    V=cfg.V)
+                self.units.append(unit)
+                self.bytes += b["total"]
+                self.elems += b["elems"]
+                self.launches += 1 + adam_launches(T, lo, hi)
+        self.hp = bq.adam_hparams(cfg.lr, cfg.b1, cfg.b2, cfg.eps, cfg.t)
+        self.name = name
+
+    def run(self, stream):
+        bq = self.bq
+        for u in self.units:
+            bq.pack(u["shard"], u["gp"], u["dbuf"], 1.0 / u["V"], False, stream=stream)
+            bq.step_adam8(u["shard"], u["dbuf"], u["master"], u["m"], u["v"], u["ms"], u["vs"], self.hp,
+                          u["fp8"], u["fs"], stream=stream)
+
+    def measure(self, stream, steps=10, warmup=3):
+        """(eager ms, graph ms) per whole-model step."""
+        torch = self.torch
+        eager = time_call(lambda: self.run(stream), stream, steps, warmup)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            self.run(stream)
+        replay = time_call(graph.replay, stream, steps, warmup)
+        self.bq.shard_check(self.units[0]["shard"], stream=stream)
+        del graph
+        return eager, replay
+
+
 def time_call(fn, stream, steps, warmup):
     """Mean milliseconds of fn() on stream (CUDA events)."""
     import torch
@@ -535,6 +608,15 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         muon_e2e = e0.elapsed_time(e1) / km
 
+    model = None
+    if args.model_step:
+        mst = ModelStep("llama3-70b-rank0", dev, seed=5000 + rank)
+        side = torch.cuda.Stream(dev)
+        with torch.cuda.stream(side):
+            model = max_over_ranks(list(mst.measure(side)), world, device=dev)
+        model_info = (mst.bytes, mst.elems, mst.launches, len(mst.units))
+        del mst
+        torch.cuda.empty_cache()
     dq = None
     if args.dequant:
         view = torch.empty(step.n, dtype=torch.bfloat16, device=dev)
@@ -599,6 +681,18 @@ def run_ours(args):
                             "e2e": {"value": round(job_throughput(muon.flops, world, muon_e2e_max) / 1e12, 1),
                                     "unit": "TFLOP/s", "h2d_bytes_per_step": muon.h2d,
                                     "d2h_bytes_per_step": muon.d2h, "ms_per_step": round(muon_e2e_max, 3)}}
+        if model:
+            eg, gr = model
+            mb, me, ml, mu = model_info
+            line["model_step"] = {
+                "workload": f"llama3-70b-rank0: all {mu} units (embedding, 80 layers, head) of the rank-0 slice at "
+                            "V=64, one DBuffer each, 128x128 Adam tiles + FP8",
+                "elements": me, "bytes": mb, "launches": ml,
+                "eager": {"ms": round(eg, 3), "GB/s": round(mb / (eg * 1e-3) / 1e9, 1)},
+                "cuda_graph": {"ms": round(gr, 3), "GB/s": round(mb / (gr * 1e-3) / 1e9, 1),
+                               "frac": round(mb / (gr * 1e-3) / 1e9 / pk["hbm"], 4)},
+                "note": "measured after the timed region; not part of value",
+            }
         if dq:
             dq_bytes = 3 * dq_elems + 4 * step.bytes["fp8_tiles"]
             gb = dq_bytes / (dq * 1e-3) / 1e9
@@ -686,6 +780,8 @@ def main():
     ap.add_argument("--muon", dest="muon", action="store_true", default=True)
     ap.add_argument("--no-muon", dest="muon", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--model-step", dest="model_step", action="store_true", default=True)
+    ap.add_argument("--no-model-step", dest="model_step", action="store_false")
     ap.add_argument("--dequant", dest="dequant", action="store_true", default=True)
     ap.add_argument("--no-dequant", dest="dequant", action="store_false")
     ap.add_argument("--tile32", dest="tile32", action="store_true", default=True)
