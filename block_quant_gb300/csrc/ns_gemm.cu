@@ -33,6 +33,12 @@ constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 e
 constexpr int TMEM_COLS = 256;     // one 128 x 256 fp32 accumulator
 constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
+// X X^T and (A A^T with A symmetric) have symmetric results: compute the tiles
+// touching the upper triangle only and mirror them
+#ifndef BQ_NS_SYMMETRIC
+#define BQ_NS_SYMMETRIC 1
+#endif
+constexpr int kSymmetric = BQ_NS_SYMMETRIC;
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -151,6 +157,7 @@ struct GemmArgs {
   __nv_bfloat16* D;        // output, row pitch ldd
   int64_t ldc, ldd;
   int* status;
+  int sym;  // D is symmetric (M == N): only tiles touching the upper triangle run, and mirror it
 };
 
 // D[M x N] = alpha * (A[M x K] . op(B)) + beta * C.  A: K-major tensor map
@@ -173,6 +180,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   const int nk = (g.K + BK - 1) / BK;
+  // symmetric output: a tile wholly below the diagonal has nothing to do (its
+  // elements are written, mirrored, by the tiles holding their transposes)
+  if (g.sym && n0 + BN <= m0) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -241,37 +251,61 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(32 * c), r);
         const int col0 = n0 + 32 * c;
         if (row >= g.M || col0 >= g.N) continue;
+        // symmetric output: this thread writes columns >= row and mirrors those > row
+        if (g.sym && col0 + 31 < row) continue;
         __nv_bfloat16* drow = g.D + int64_t(row) * g.ldd;
         const __nv_bfloat16* crow = g.C ? g.C + int64_t(row) * g.ldc : nullptr;
-        const bool vec = col0 + 32 <= g.N && ((reinterpret_cast<uintptr_t>(drow + col0) | (crow ? reinterpret_cast<uintptr_t>(crow + col0) : 0)) & 15) == 0;
-        if (vec) {
+        const bool cterm = crow && g.beta != 0.f;
+        const bool cvec = cterm && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(crow + col0) & 15) == 0;
+        __nv_bfloat162 o2[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float cv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          if (cvec) {
+            const uint4 cw = *reinterpret_cast<const uint4*>(crow + col0 + 8 * v);
+            const __nv_bfloat162* cp = reinterpret_cast<const __nv_bfloat162*>(&cw);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f = __bfloat1622float2(cp[j]);
+              cv[2 * j] = f.x;
+              cv[2 * j + 1] = f.y;
+            }
+          } else if (cterm) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (col0 + 8 * v + j < g.N) cv[j] = __bfloat162float(crow[col0 + 8 * v + j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = g.alpha * __uint_as_float(r[8 * v + 2 * j]) + g.beta * cv[2 * j];
+            const float hi = g.alpha * __uint_as_float(r[8 * v + 2 * j + 1]) + g.beta * cv[2 * j + 1];
+            o2[4 * v + j] = __floats2bfloat162_rn(lo, hi);
+          }
+        }
+        const bool whole = !g.sym || col0 >= row;  // every column of the chunk is written directly
+        if (whole && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(drow + col0) & 15) == 0) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            float cv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (crow && g.beta != 0.f) {
-              const uint4 cw = *reinterpret_cast<const uint4*>(crow + col0 + 8 * v);
-              const __nv_bfloat162* cp = reinterpret_cast<const __nv_bfloat162*>(&cw);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float2 f = __bfloat1622float2(cp[j]);
-                cv[2 * j] = f.x;
-                cv[2 * j + 1] = f.y;
-              }
-            }
             uint4 ow;
             __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ow);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float lo = g.alpha * __uint_as_float(r[8 * v + 2 * j]) + g.beta * cv[2 * j];
-              const float hi = g.alpha * __uint_as_float(r[8 * v + 2 * j + 1]) + g.beta * cv[2 * j + 1];
-              op[j] = __floats2bfloat162_rn(lo, hi);
-            }
+            for (int j = 0; j < 4; ++j) op[j] = o2[4 * v + j];
             *reinterpret_cast<uint4*>(drow + col0 + 8 * v) = ow;
           }
         } else {
-          for (int j = 0; j < 32 && col0 + j < g.N; ++j) {
-            const float cv = (crow && g.beta != 0.f) ? __bfloat162float(crow[col0 + j]) : 0.f;
-            drow[col0 + j] = __float2bfloat16_rn(g.alpha * __uint_as_float(r[j]) + g.beta * cv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = col0 + j;
+            if (col < g.N && (!g.sym || col >= row)) drow[col] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
+          }
+        }
+        if (g.sym) {
+          // mirror: for one column the warp's lanes hold consecutive rows, so
+          // these stores are contiguous across the warp
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = col0 + j;
+            if (col > row && col < g.N) g.D[int64_t(col) * g.ldd + row] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
           }
         }
       }
@@ -517,13 +551,13 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
     for (int it = 0; it < steps; ++it) {
       const int nxt = cur ^ 1;
       // A = X X^T
-      GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status};
+      GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status, kSymmetric};
       if (int rc = gemm(false, mXa[cur], mXb[cur], g1, s)) return rc;
       // B = c (A A^T) + b A   (A symmetric)
-      GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status};
+      GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric};
       if (int rc = gemm(false, mAa, mAb, g2, s)) return rc;
       // X' = B X + a X
-      GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status};
+      GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0};
       if (int rc = gemm(true, mBa, mXmn[cur], g3, s)) return rc;
       cur = nxt;
     }
