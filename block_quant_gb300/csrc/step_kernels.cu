@@ -846,16 +846,27 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGrou
     const int nvec = g.rows * vpr;
     const int slot = g.mslot + warp;
     const float sm = a.m_scale[slot], sv = a.v_scale[slot];
-    uint32_t am = 0, av = 0;
-    for (int v = lane; v < nvec; v += 32) {
+    auto vpos = [&](int v) {
       const int r = v / vpr, k = v - r * vpr;
-      const int64_t pos = g.pos + int64_t(r) * g.C + c + (k << 3);
-      const Raw8 x = raw_from_global(a, pos, 8);
+      return g.pos + int64_t(r) * g.C + c + (k << 3);
+    };
+    uint32_t am = 0, av = 0;
+    for (int v = lane; v < nvec; v += 64) {
+      const bool two = v + 32 < nvec;
+      const int64_t p0 = vpos(v), p1 = two ? vpos(v + 32) : p0;
+      const Raw8 x0 = raw_from_global(a, p0, 8);
+      const Raw8 x1 = raw_from_global(a, p1, two ? 8 : 0);
       Lane8 o;
-      adam_raw<true>(h, x, 8, sm, sv, o);
-      store_p8(a.master + pos, o.p1);
+      adam_raw<true>(h, x0, 8, sm, sv, o);
+      store_p8(a.master + p0, o.p1);
       am = max(am, o.am);
       av = max(av, o.av);
+      if (two) {
+        adam_raw<true>(h, x1, 8, sm, sv, o);
+        store_p8(a.master + p1, o.p1);
+        am = max(am, o.am);
+        av = max(av, o.av);
+      }
     }
     QScale qm, qv;
     warp_block_scales(am, av, lane, qm, qv);
@@ -864,13 +875,12 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGrou
       a.v_scale[slot] = qv.s;
     }
     for (int v = lane; v < nvec; v += 32) {
-      const int r = v / vpr, k = v - r * vpr;
-      const int64_t pos = g.pos + int64_t(r) * g.C + c + (k << 3);
+      const int64_t pos = vpos(v);
       Raw8 x;
       x.g = *reinterpret_cast<const uint4*>(a.grad + pos);
       x.m = *reinterpret_cast<const uint2*>(a.m + pos);
       x.v = *reinterpret_cast<const uint2*>(a.v + pos);
-      x.p0 = x.p1 = make_float4(0.f, 0.f, 0.f, 0.f);  // p' is not needed here
+      x.p0 = x.p1 = make_float4(0.f, 0.f, 0.f, 0.f);
       Lane8 o;
       adam_raw<true>(h, x, 8, sm, sv, o);
       *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);

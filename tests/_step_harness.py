@@ -14,6 +14,7 @@ from oracle import planner as P
 
 PAD_F32 = np.float32(1234.5)  # sentinels in padding: must survive the step
 PAD_I8, PAD_U8 = np.int8(77), np.uint8(77)
+GUARD_BYTES = 1024  # canary tail after every device buffer
 
 
 class StepCase:
@@ -69,7 +70,17 @@ class StepCase:
 
     # ------------------------------------------------------------------ CUDA path
     def run_gpu(self, dev, scale=None, accumulate=False, fp8=True, reps=1):
-        d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        # every device buffer gets a canary tail: a write past the end of any
+        # output shows up as a changed tail (the sanitizer stand-in)
+        guards = []
+
+        def d(a):
+            a = np.ascontiguousarray(a)
+            tail = np.frombuffer(np.full(GUARD_BYTES, 0x5A, np.uint8).tobytes(), dtype=a.dtype)
+            full = torch.from_numpy(np.concatenate([a.reshape(-1), tail])).to(dev)
+            guards.append((full, a.size))
+            return full[:a.size]
+
         s = torch.cuda.current_stream(dev)
         ws = torch.empty(self.layout.upload_bytes(self.dev_lo, self.dev_hi), dtype=torch.uint8, device=dev)
         shard = self.layout.upload(self.dev_lo, self.dev_hi, ws, stream=s)
@@ -94,6 +105,9 @@ class StepCase:
         bq.quant_fp8(shard, master, q2, s2, stream=s)
         bq.shard_check(shard, stream=s)  # no bounded device wait gave up
         torch.cuda.synchronize(dev)
+        for full, n in guards:
+            tail = full[n:].cpu().numpy().view(np.uint8)
+            assert np.all(tail == 0x5A), f"write past the end of a {n}-element buffer"
         h = lambda t: None if t is None else t.cpu().numpy()  # noqa: E731
         out = dict(dbuf=h(dbuf).view(np.uint16), master=h(master), m=h(m), v=h(v), ms=h(ms), vs=h(vs),
                    fp8=h(fp8_out), fs=h(fs), q2=h(q2), s2=h(s2))
