@@ -780,16 +780,31 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
     const float sm = a.m_scale[g.mslot], sv = a.v_scale[g.mslot];
     const int vpr = g.width >> 3, nvec = g.rows * vpr;
     uint32_t am = 0, av = 0, ap = 0;
-    for (int v = threadIdx.x; v < nvec; v += kThreads) {
-      const int r = v / vpr, k = v - r * vpr;
-      const int64_t pos = g.pos + int64_t(r) * g.C + (k << 3);
-      const Raw8 x = raw_from_global(a, pos, 8);
+    for (int v = threadIdx.x; v < nvec; v += 2 * kThreads) {
+      // two vectors' loads in flight per thread
+      const bool two = v + kThreads < nvec;
+      const int r0 = v / vpr, k0 = v - r0 * vpr;
+      const int64_t pos0 = g.pos + int64_t(r0) * g.C + (k0 << 3);
+      int64_t pos1 = pos0;
+      if (two) {
+        const int r1 = (v + kThreads) / vpr, k1 = (v + kThreads) - r1 * vpr;
+        pos1 = g.pos + int64_t(r1) * g.C + (k1 << 3);
+      }
+      const Raw8 x0 = raw_from_global(a, pos0, 8);
+      const Raw8 x1 = raw_from_global(a, pos1, two ? 8 : 0);
       Lane8 o;
-      adam_raw<true>(h, x, 8, sm, sv, o);
-      store_p8(a.master + pos, o.p1);
+      adam_raw<true>(h, x0, 8, sm, sv, o);
+      store_p8(a.master + pos0, o.p1);
       am = max(am, o.am);
       av = max(av, o.av);
       ap = max(ap, o.ap);
+      if (two) {
+        adam_raw<true>(h, x1, 8, sm, sv, o);
+        store_p8(a.master + pos1, o.p1);
+        am = max(am, o.am);
+        av = max(av, o.av);
+        ap = max(ap, o.ap);
+      }
     }
     block_max(am, red, 0);
     block_max(av, red, 1);
