@@ -2,19 +2,24 @@
 //   k_pack         fused pre-communication copy / scale / add / zero into the
 //                  bf16 gradient DBuffer (DBuffer's group-level pre-comm ops,
 //                  veScale-FSDP bud-325 summary, Key claims and Method)
-//   k_flat<E>      8-bit Adam over runs of flat blocks (256 or 128 elements),
+//   k_flat<E>      8-bit Adam over runs of flat blocks (256, 128 or 32 elements),
 //                  optionally fused with 1x128 FP8 tiles of 1-D tensors
 //   k_strip<FP8>   8-bit Adam with flat 256-element blocks over a 2-D region,
-//                  fused with 128x128 FP8 tiles (two phases, tile amax in smem)
+//                  fused with 128x128 FP8 tiles; inputs staged by a producer
+//                  warp's bulk (TMA) copies, tile amax in shared memory
 //   k_tile<FP8>    8-bit Adam with 128x128 state tiles (+ FP8 of the same tile)
+//   k_tile32       8-bit Adam with the pages' 32x32 state tiles
 //   k_quant_*      standalone FP8 requantisation
+//   k_dequant_*    the bf16 view (code x tile scale) of the gathered FP8 buffer
+//   k_muon_*       Muon's momentum + gather and apply around Newton-Schulz
 // The 8-bit Adam is the pages' block-quantised optimizer state kept local to a
 // shard (feynmanwiki walkthrough, paper section 6.3); FP8 is block-wise FP8 in
 // the DeepSeek-V3 style (bud-325 TL;DR).
 //
-// Every value-producing fp32 operation uses an explicit round-to-nearest
-// intrinsic (no contraction into FMA), in the order the host-side contract fixes,
-// so codes, scales and master weights are reproducible bit for bit.
+// Every value-producing fp32 operation is an explicit round-to-nearest
+// intrinsic or an explicit fused multiply-add (compiled with -fmad=false, so
+// nothing else is contracted), in the order the host-side contract fixes, so
+// codes, scales and master weights are reproducible bit for bit.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
