@@ -40,6 +40,7 @@ constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
 #endif
 constexpr int kSymmetric = BQ_NS_SYMMETRIC;
 
+
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -178,7 +179,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  // tile order: the MN-major product (B X) runs row blocks fastest, so the CTAs
+  // resident at once share a few column blocks of X and all of B, which stay in
+  // L2; the other products run column blocks fastest
+  const int m0 = (B_MN ? blockIdx.x : blockIdx.y) * BM, n0 = (B_MN ? blockIdx.y : blockIdx.x) * BN;
   const int nk = (g.K + BK - 1) / BK;
   // symmetric output: a tile wholly below the diagonal has nothing to do (its
   // elements are written, mirrored, by the tiles holding their transposes)
@@ -481,7 +485,8 @@ int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs
     cudaFuncSetAttribute(k_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
     cudaFuncSetAttribute(k_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
   });
-  const dim3 grid(unsigned((g.N + BN - 1) / BN), unsigned((g.M + BM - 1) / BM));
+  const unsigned mt = unsigned((g.M + BM - 1) / BM), nt = unsigned((g.N + BN - 1) / BN);
+  const dim3 grid = b_mn ? dim3(mt, nt) : dim3(nt, mt);
   if (b_mn)
     k_gemm<true><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, g);
   else
