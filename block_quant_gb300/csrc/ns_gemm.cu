@@ -369,26 +369,75 @@ __global__ void __launch_bounds__(kRedThreads) k_inv_norm(const float* __restric
 // out = x * (*inv) (transposed when `transpose`; inv NULL: plain copy), out row
 // pitch ldo.  32 x 32
 // tiles through shared memory so both sides stay coalesced.
+// out = bf16(x * s) (s = *inv, or 1), optionally transposed; 64 x 64 tiles, eight
+// elements per thread access (16-byte vectors where the rows allow), the
+// transpose through a shared-memory tile
+constexpr int kCopyTile = 64;
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* __restrict__ x, int64_t r, int64_t c, int64_t rows,
+                                      int64_t cols, int64_t ldx, bool vec, float s, float* v) {
+  if (r < rows && vec && c + 8 <= cols) {
+    const uint4 w = *reinterpret_cast<const uint4*>(x + r * ldx + c);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      v[2 * e] = f.x * s;
+      v[2 * e + 1] = f.y * s;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = (r < rows && c + e < cols) ? __bfloat162float(x[r * ldx + c + e]) * s : 0.f;
+  }
+}
+
+__device__ __forceinline__ void store8(__nv_bfloat16* __restrict__ out, int64_t r, int64_t c, int64_t rows,
+                                       int64_t cols, int64_t ldo, bool vec, const float* v) {
+  if (r >= rows) return;
+  if (vec && c + 8 <= cols) {
+    uint4 w;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+    *reinterpret_cast<uint4*>(out + r * ldo + c) = w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (c + e < cols) out[r * ldo + c + e] = __float2bfloat16_rn(v[e]);
+  }
+}
+
 __global__ void __launch_bounds__(256) k_scale_copy(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols,
                                                    int64_t ldx, __nv_bfloat16* __restrict__ out, int64_t ldo,
                                                    int transpose, const float* __restrict__ inv) {
   const float s = inv ? *inv : 1.f;
-  __shared__ float tile[32][33];
-  const int64_t r0 = int64_t(blockIdx.y) * 32, c0 = int64_t(blockIdx.x) * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  for (int i = ty; i < 32; i += 8) {
-    const int64_t r = r0 + i, c = c0 + tx;
-    tile[i][tx] = (r < rows && c < cols) ? __bfloat162float(x[r * ldx + c]) * s : 0.f;
-  }
-  __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    if (transpose) {
-      const int64_t orow = c0 + i, ocol = r0 + tx;  // out is cols x rows
-      if (orow < cols && ocol < rows) out[orow * ldo + ocol] = __float2bfloat16_rn(tile[tx][i]);
+  __shared__ float tile[kCopyTile][kCopyTile + 1];
+  const int64_t r0 = int64_t(blockIdx.y) * kCopyTile, c0 = int64_t(blockIdx.x) * kCopyTile;
+  const int t = threadIdx.x;
+  const bool vin = (ldx & 7) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  const bool vout = (ldo & 7) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int i = (t >> 3) + 32 * pass, j = (t & 7) << 3;  // 8 threads per 64-element row
+    float v[8];
+    load8(x, r0 + i, c0 + j, rows, cols, ldx, vin, s, v);
+    if (!transpose) {
+      store8(out, r0 + i, c0 + j, rows, cols, ldo, vout, v);
     } else {
-      const int64_t r = r0 + i, c = c0 + tx;
-      if (r < rows && c < cols) out[r * ldo + c] = __float2bfloat16_rn(tile[i][tx]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tile[i][j + e] = v[e];
     }
+  }
+  if (!transpose) return;  // uniform
+  __syncthreads();
+  // out is cols x rows: its row c0 + i holds tile column i
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int i = (t >> 3) + 32 * pass, j = (t & 7) << 3;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = tile[j + e][i];
+    store8(out, c0 + i, r0 + j, cols, rows, ldo, vout, v);
   }
 }
 
@@ -534,7 +583,7 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
     // normalise into X0 (transposed for a tall input)
     k_sumsq<<<kRedBlocks, kRedThreads, 0, s>>>(x, t.rows, t.cols, t.ld_x, part);
     if (int rc = check("bq_muon_ns (norm)")) return rc;
-    const dim3 cg(unsigned((t.cols + 31) / 32), unsigned((t.rows + 31) / 32));
+    const dim3 cg(unsigned((t.cols + kCopyTile - 1) / kCopyTile), unsigned((t.rows + kCopyTile - 1) / kCopyTile));
     k_inv_norm<<<1, kRedThreads, 0, s>>>(part, kRedBlocks, eps, inv);
     if (int rc = check("bq_muon_ns (inv norm)")) return rc;
     k_scale_copy<<<cg, 256, 0, s>>>(x, t.rows, t.cols, t.ld_x, X0, p.ldx, p.tall ? 1 : 0, inv);
@@ -567,7 +616,7 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
       cur = nxt;
     }
     // y = X (transposed back for a tall input)
-    const dim3 og(unsigned((p.n + 31) / 32), unsigned((p.m + 31) / 32));
+    const dim3 og(unsigned((p.n + kCopyTile - 1) / kCopyTile), unsigned((p.m + kCopyTile - 1) / kCopyTile));
     k_scale_copy<<<og, 256, 0, s>>>(Xs[cur], p.m, p.n, p.ldx, y, t.ld_y, p.tall ? 1 : 0, nullptr);
     if (int rc = check("bq_muon_ns (copy out)")) return rc;
   }
