@@ -692,15 +692,16 @@ def run_ours(args):
         muon.pin_host()
         muon_e2e = muon.measure_e2e(stream)
 
-    model = None
+    models = {}
     if args.model_step:
-        mst = ModelStep("llama3-70b-rank0", dev, seed=5000 + rank)
-        side = torch.cuda.Stream(dev)
-        with torch.cuda.stream(side):
-            model = max_over_ranks(list(mst.measure(side)), world, device=dev)
-        model_info = (mst.bytes, mst.elems, mst.launches, len(mst.units))
-        del mst
-        torch.cuda.empty_cache()
+        for mname in ("llama3-70b-rank0", "gpt-oss-120b-rank0"):
+            mst = ModelStep(mname, dev, seed=5000 + rank)
+            side = torch.cuda.Stream(dev)
+            with torch.cuda.stream(side):
+                res = max_over_ranks(list(mst.measure(side)), world, device=dev)
+            models[mname] = (res, (mst.bytes, mst.elems, mst.launches, len(mst.units)))
+            del mst
+            torch.cuda.empty_cache()
     dq = None
     if args.dequant:
         view = torch.empty(step.n, dtype=torch.bfloat16, device=dev)
@@ -771,12 +772,14 @@ def run_ours(args):
                             "e2e": {"value": round(job_throughput(muon.flops, world, muon_e2e_max) / 1e12, 1),
                                     "unit": "TFLOP/s", "h2d_bytes_per_step": muon.h2d,
                                     "d2h_bytes_per_step": muon.d2h, "ms_per_step": round(muon_e2e_max, 3)}}
-        if model:
-            eg, gr = model
-            mb, me, ml, mu = model_info
-            line["model_step"] = {
-                "workload": f"llama3-70b-rank0: all {mu} units (embedding, 80 layers, head) of the rank-0 slice at "
-                            "V=64, one DBuffer each, 128x128 Adam tiles + FP8",
+        desc = {"llama3-70b-rank0": "all {u} units (embedding, 80 layers, head) of the rank-0 slice at V=64, one "
+                                    "DBuffer each, 128x128 Adam tiles + FP8",
+                "gpt-oss-120b-rank0": "all {u} units (embedding, 36 MoE layers, head) of the rank-0 slice at V=256, "
+                                      "one DBuffer each, 256-element Adam blocks + 128x128 FP8 (d = 2880: whole-band "
+                                      "regions)"}
+        for mname, ((eg, gr), (mb, me, ml, mu)) in models.items():
+            line.setdefault("model_step", {})[mname] = {
+                "workload": f"{mname}: " + desc[mname].format(u=mu),
                 "elements": me, "bytes": mb, "launches": ml,
                 "eager": {"ms": round(eg, 3), "GB/s": round(mb / (eg * 1e-3) / 1e9, 1)},
                 "cuda_graph": {"ms": round(gr, 3), "GB/s": round(mb / (gr * 1e-3) / 1e9, 1),

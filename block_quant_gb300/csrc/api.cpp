@@ -51,8 +51,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsPlan {
-  size_t off_pieces, off_chunks, off_f256, off_f128, off_strips, off_tiles, off_muon, off_f32, off_t32, off_status,
-      bytes;
+  size_t off_pieces, off_chunks, off_f256, off_f128, off_strips, off_tiles, off_muon, off_f32, off_t32, off_bt,
+      off_status, bytes;
 };
 
 WsPlan ws_plan(const ShardTables& T) {
@@ -76,6 +76,8 @@ WsPlan ws_plan(const ShardTables& T) {
   o = align_up(o + T.flat32.size() * sizeof(FlatGroup), 256);
   p.off_t32 = o;
   o = align_up(o + T.tiles32.size() * sizeof(RegionGroup), 256);
+  p.off_bt = o;
+  o = align_up(o + T.band_tiles.size() * sizeof(RegionGroup), 256);
   p.off_status = o;  // device error word, zeroed by the upload
   o += 256;
   p.bytes = o;
@@ -153,6 +155,7 @@ int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, s
   put(p.off_muon, T.muon.data(), T.muon.size() * sizeof(PackPiece));
   put(p.off_f32, T.flat32.data(), T.flat32.size() * sizeof(FlatGroup));
   put(p.off_t32, T.tiles32.data(), T.tiles32.size() * sizeof(RegionGroup));
+  put(p.off_bt, T.band_tiles.data(), T.band_tiles.size() * sizeof(RegionGroup));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(dev_ws, img.data(), p.bytes, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -175,6 +178,7 @@ int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, s
   sh->dev.muon = reinterpret_cast<const PackPiece*>(base + p.off_muon);
   sh->dev.flat32 = reinterpret_cast<const FlatGroup*>(base + p.off_f32);
   sh->dev.tiles32 = reinterpret_cast<const RegionGroup*>(base + p.off_t32);
+  sh->dev.band_tiles = reinterpret_cast<const RegionGroup*>(base + p.off_bt);
   sh->dev.nchunks = T.nchunks;
   sh->dev.n_flat256 = int32_t(T.flat256.size());
   sh->dev.n_flat128 = int32_t(T.flat128.size());
@@ -183,6 +187,7 @@ int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, s
   sh->dev.n_muon = int32_t(T.muon.size());
   sh->dev.n_flat32 = int32_t(T.flat32.size());
   sh->dev.n_tiles32 = int32_t(T.tiles32.size());
+  sh->dev.n_band_tiles = int32_t(T.band_tiles.size());
   sh->dev.max_strip_tiles = T.max_strip_tiles;
   sh->dev.status = reinterpret_cast<int*>(base + p.off_status);
   *out = sh;

@@ -101,6 +101,7 @@ struct ShardTables {
   std::vector<PackPiece> muon;        // Muon tensors: dst local, src tensor offset, <= 8192 elements
   std::vector<FlatGroup> flat32;      // TILE32 Adam on 1-D tensors (32-element blocks)
   std::vector<RegionGroup> tiles32;   // TILE32 Adam on 2-D tensors: 32-row band x <= 256 columns
+  std::vector<RegionGroup> band_tiles;  // FP8 tiles of FLAT256 tensors with C % 256 != 0 (one group each)
   int64_t nchunks = 0;
   int32_t max_strip_tiles = 0;        // most FP8 column tiles in one strip group
 };
@@ -120,8 +121,9 @@ struct DevTables {
   const PackPiece* muon;
   const FlatGroup* flat32;
   const RegionGroup* tiles32;
+  const RegionGroup* band_tiles;
   int64_t nchunks;
-  int32_t n_flat256, n_flat128, n_strips, n_tiles, n_muon, n_flat32, n_tiles32;
+  int32_t n_flat256, n_flat128, n_strips, n_tiles, n_muon, n_flat32, n_tiles32, n_band_tiles;
   int32_t max_strip_tiles;
   int* status;  // device error word: 0, or the site of a wait that timed out
 };

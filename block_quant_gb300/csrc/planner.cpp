@@ -354,8 +354,10 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
   T.muon.clear();
   T.flat32.clear();
   T.tiles32.clear();
+  T.band_tiles.clear();
   T.max_strip_tiles = 0;
   constexpr int64_t kFlatGroupElems = 8192;
+  constexpr int64_t kBandPiece = 32768;  // whole 256-element blocks
   for (int64_t k = first; k < last; ++k) {
     const Interval& v = L.intervals[k];
     const Tensor& t = L.tensors[v.tensor];
@@ -431,8 +433,21 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
                                              int32_t(mband + c0 / 256), int32_t(fband + c0 / 128), cmul, cshr});
             T.max_strip_tiles = std::max(T.max_strip_tiles, 2);
           } else {
-            T.strips.push_back(RegionGroup{bpos, rows, int32_t(C), 0, int32_t(C), mband, fband, cmul, cshr});
-            T.max_strip_tiles = std::max<int32_t>(T.max_strip_tiles, int32_t(nct));
+            // whole 128-row bands (256-element Adam blocks cross rows): Adam over
+            // flat pieces of the band (a flat region of one row: rows = 1,
+            // width = C = length, no FP8), and one group per FP8 tile for the
+            // two-pass quantiser, so a band spreads over many CTAs
+            const int64_t nel = int64_t(rows) * C;
+            for (int64_t e0 = 0; e0 < nel; e0 += kBandPiece) {
+              const int32_t len = int32_t(std::min(kBandPiece, nel - e0));
+              T.strips.push_back(RegionGroup{bpos + e0, 1, len, 0, len, int32_t(mband + e0 / 256), -1, 0, 0});
+            }
+            for (int64_t ct = 0; ct < nct; ++ct) {
+              const int64_t c0 = ct * 128;
+              T.band_tiles.push_back(RegionGroup{bpos + c0, rows, int32_t(C), int32_t(c0),
+                                                 int32_t(std::min<int64_t>(128, C - c0)), 0, int32_t(fband + ct),
+                                                 cmul, cshr});
+            }
           }
         }
       }
@@ -486,8 +501,16 @@ std::string validate_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, co
     const int64_t mend = flat ? g.mslot + ceil_div(int64_t(g.rows) * g.C, 256)
                               : g.mslot + int64_t(g.rows - 1) * (g.C / 256) + g.width / 256;
     if (g.mslot < 0 || mend > nm) return "strip Adam slots out of range";
-    if (g.fslot < 0 || g.fslot + ceil_div(g.width, 128) > nf) return "strip FP8 slots out of range";
-    if (ceil_div(g.width, 128) > T.max_strip_tiles) return "strip tile count above the shared-memory bound";
+    if (g.fslot < 0 && !flat) return "2-D strip without FP8 slots";
+    if (g.fslot >= 0 && g.fslot + ceil_div(g.width, 128) > nf) return "strip FP8 slots out of range";
+    if (g.fslot >= 0 && ceil_div(g.width, 128) > T.max_strip_tiles) return "strip tile count above the shared-memory bound";
+  }
+  for (const RegionGroup& g : T.band_tiles) {
+    if (g.rows <= 0 || g.rows > 128 || g.width <= 0 || g.width > 128 || g.width % 8 || g.C % 8 || g.pos % 8 ||
+        g.pos < 0 || g.c0 + g.width > g.C || (g.width == g.C && g.c0 != 0))
+      return "band FP8 tile shape";
+    if (g.pos + int64_t(g.rows - 1) * g.C + g.width > total) return "band FP8 tile outside the shard range";
+    if (g.fslot < 0 || g.fslot >= nf) return "band FP8 tile slot out of range";
   }
   for (const PackPiece& p : T.muon) {
     if (p.len <= 0 || p.dst < 0 || p.dst + p.len > total) return "Muon piece outside the shard range";

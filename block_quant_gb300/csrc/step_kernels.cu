@@ -648,10 +648,11 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
   for (int gi = ngroups - 1 - int(blockIdx.x); gi >= 0; gi -= int(gridDim.x)) {
     const RegionGroup g = groups[gi];
     const bool flat = g.width == g.C;
+    const bool fp8 = FP8 && g.fslot >= 0;  // band pieces carry no FP8 (their tiles are quantised apart)
     const int ntile = (g.width + 127) >> 7;
     const int nel = g.rows * g.width;
     const int nblk = region_blocks(g);
-    if (FP8) {
+    if (fp8) {
       for (int t = threadIdx.x; t < ntile; t += kCT) s_tile[t] = 0u;
       consumer_sync();
     }
@@ -697,7 +698,7 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
         a.m_scale[slot] = qm.s;
         a.v_scale[slot] = qv.s;
       }
-      if (FP8) {
+      if (fp8) {
         if (flat) {
           // column of the lane's first element; several lanes share a tile
           const uint32_t e = uint32_t((b << 8) + lane * 8);
@@ -713,7 +714,7 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
         }
       }
     }
-    if (FP8) {
+    if (fp8) {
       consumer_sync();
       if (!dead) {
         for (int t = threadIdx.x; t < ntile; t += kCT) {
@@ -1208,6 +1209,13 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
       k_strip<false><<<grid, kStripThreads, smem, s>>>(t.strips, t.n_strips, a);
     if (int rc = check_launch("bq_step_adam8 (strips)")) return rc;
   }
+  if (fp8 && t.n_band_tiles) {
+    // FP8 of tensors whose Adam ran as band pieces: two passes per tile over the
+    // just-written master (L2)
+    k_quant_region<<<std::min(t.n_band_tiles, sms * 8), kThreads, 2 * sizeof(uint32_t), s>>>(
+        t.band_tiles, t.n_band_tiles, a.master, a.fp8, a.fp8_scale);
+    if (int rc = check_launch("bq_step_adam8 (band FP8 tiles)")) return rc;
+  }
   if (t.n_tiles) {
     const int grid = std::min(t.n_tiles, sms * kTileCtasPerSm);
     if (fp8)
@@ -1237,6 +1245,11 @@ int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, floa
                                                                                         fp8, fp8_scale);
     if (int rc = check_launch("bq_quant_fp8 (strips)")) return rc;
   }
+  if (t.n_band_tiles) {
+    k_quant_region<<<std::min(t.n_band_tiles, sms * 8), kThreads, 2 * sizeof(uint32_t), s>>>(
+        t.band_tiles, t.n_band_tiles, master, fp8, fp8_scale);
+    if (int rc = check_launch("bq_quant_fp8 (band tiles)")) return rc;
+  }
   if (t.n_tiles) {
     k_quant_region<<<std::min(t.n_tiles, sms * kTileCtasPerSm), kThreads, 2 * sizeof(uint32_t), s>>>(
         t.tiles, t.n_tiles, master, fp8, fp8_scale);
@@ -1263,6 +1276,11 @@ int launch_dequant_fp8(const DevTables& t, const uint8_t* fp8, const float* fp8_
   if (t.n_tiles) {
     k_dequant_region<<<std::min(t.n_tiles, sms * 8), kThreads, 0, s>>>(t.tiles, t.n_tiles, fp8, fp8_scale, out);
     if (int rc = check_launch("bq_dequant_fp8 (tiles)")) return rc;
+  }
+  if (t.n_band_tiles) {
+    k_dequant_region<<<std::min(t.n_band_tiles, sms * 8), kThreads, 0, s>>>(t.band_tiles, t.n_band_tiles, fp8,
+                                                                           fp8_scale, out);
+    if (int rc = check_launch("bq_dequant_fp8 (band tiles)")) return rc;
   }
   return BQ_OK;
 }
