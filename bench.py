@@ -702,6 +702,9 @@ def run_ours(args):
             models[mname] = (res, (mst.bytes, mst.elems, mst.launches, len(mst.units)))
             del mst
             torch.cuda.empty_cache()
+    acc_ms = max_over_ranks([time_call(lambda: bq.pack(step.shard, step.gptrs, step.dbuf, 1.0 / step.V, True,
+                                                       stream=stream), stream, steps=20, warmup=3)],
+                            world, device=dev)[0]
     dq = None
     if args.dequant:
         view = torch.empty(step.n, dtype=torch.bfloat16, device=dev)
@@ -786,6 +789,14 @@ def run_ours(args):
                                "frac": round(mb / (gr * 1e-3) / 1e9 / pk["hbm"], 4)},
                 "note": "measured after the timed region; not part of value",
             }
+        acc_bytes = 6 * step.bytes["elems"] + 2 * step.bytes["pads"]
+        line["pack_accumulate"] = {
+            "workload": "llama3-8b-layer pack with accumulation into the gradient DBuffer (read grad 2 + DBuffer 2, "
+                        "write 2 per element; padding zeroed), all 8 shards",
+            "ms": round(acc_ms, 4), "GB/s": round(acc_bytes / (acc_ms * 1e-3) / 1e9, 1),
+            "frac": round(acc_bytes / (acc_ms * 1e-3) / 1e9 / pk["hbm"], 4), "bytes": acc_bytes,
+            "note": "measured after the timed region; not part of value",
+        }
         if dq:
             dq_bytes = 3 * dq_elems + 4 * step.bytes["fp8_tiles"]
             gb = dq_bytes / (dq * 1e-3) / 1e9

@@ -502,6 +502,9 @@ std::string validate_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, co
                               : g.mslot + int64_t(g.rows - 1) * (g.C / 256) + g.width / 256;
     if (g.mslot < 0 || mend > nm) return "strip Adam slots out of range";
     if (g.fslot < 0 && !flat) return "2-D strip without FP8 slots";
+    // FP8 regions are 256-column strips (a 256-column tensor's strip is also its
+    // whole band, where both readings of the geometry agree)
+    if (g.fslot >= 0 && g.width != 256) return "FP8 region that is not a 256-column strip";
     if (g.fslot >= 0 && g.fslot + ceil_div(g.width, 128) > nf) return "strip FP8 slots out of range";
     if (g.fslot >= 0 && ceil_div(g.width, 128) > T.max_strip_tiles) return "strip tile count above the shared-memory bound";
   }

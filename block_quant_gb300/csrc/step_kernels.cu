@@ -699,19 +699,9 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
         a.v_scale[slot] = qv.s;
       }
       if (fp8) {
-        if (flat) {
-          // column of the lane's first element; several lanes share a tile
-          const uint32_t e = uint32_t((b << 8) + lane * 8);
-          const int col = int(e - fastdiv(e, g.cmul, g.cshr) * uint32_t(g.C));
-          const int t = col >> 7;
-          const unsigned same = __match_any_sync(0xFFFFFFFFu, t);
-          const uint32_t ap = __reduce_max_sync(same, o.ap);
-          if (lane == __ffs(same) - 1) atomicMax(&s_tile[t], ap);
-        } else {
-          // strip: lanes 0-15 cover tile 0, lanes 16-31 tile 1
-          const uint32_t ap = __reduce_max_sync(lane < 16 ? 0x0000FFFFu : 0xFFFF0000u, o.ap);
-          if ((lane & 15) == 0) atomicMax(&s_tile[lane >> 4], ap);
-        }
+        // a strip row: lanes 0-15 cover column tile 0, lanes 16-31 tile 1
+        const uint32_t ap = __reduce_max_sync(lane < 16 ? 0x0000FFFFu : 0xFFFF0000u, o.ap);
+        if ((lane & 15) == 0) atomicMax(&s_tile[lane >> 4], ap);
       }
     }
     if (fp8) {
@@ -725,40 +715,29 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
         }
       }
       consumer_sync();
-      const int nvec = dead ? 0 : nel >> 3;
-      constexpr int U = 1;
-      for (int v0 = threadIdx.x; v0 < nvec; v0 += kCT * U) {
-        float4 p0[U], p1[U];
-        int64_t pos[U];
-        int tile[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + u * kCT;
-          if (v < nvec) {
-            if (flat) {
-              const uint32_t e = uint32_t(v) << 3;
-              tile[u] = int(e - fastdiv(e, g.cmul, g.cshr) * uint32_t(g.C)) >> 7;
-              pos[u] = g.pos + e;
-            } else {
-              const int r = v >> 5, kk = v & 31;  // 32 vectors of 8 per 256-column row
-              tile[u] = kk >> 4;
-              pos[u] = g.pos + int64_t(r) * g.C + (kk << 3);
-            }
-            p0[u] = *reinterpret_cast<const float4*>(a.master + pos[u]);
-            p1[u] = *reinterpret_cast<const float4*>(a.master + pos[u] + 4);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + u * kCT;
-          if (v < nvec) {
-            QScale q;
-            q.r = __uint_as_float(s_tile[tile[u]]);
-            q.s = __uint_as_float(s_tile[ntile + tile[u]]);
-            q.mode = q.s == 0.f ? 0 : (isinf(q.r) ? 2 : 1);
-            const float pv[8] = {p0[u].x, p0[u].y, p0[u].z, p0[u].w, p1[u].x, p1[u].y, p1[u].z, p1[u].w};
-            *reinterpret_cast<uint2*>(a.fp8 + pos[u]) = codes_e4m3(pv, q);
-          }
+      // each thread converts two adjacent 8-element vectors of a strip row (one
+      // 128-column tile) per pass: 128 rows x 16 pairs
+      const int npair = dead ? 0 : nel >> 4;
+      for (int q = threadIdx.x; q < npair; q += kCT) {
+        const int r = q >> 4, kk = (q & 15) << 1;  // row, first of the two vectors
+        const int64_t pos = g.pos + int64_t(r) * g.C + (kk << 3);
+        const float4 p0 = *reinterpret_cast<const float4*>(a.master + pos);
+        const float4 p1 = *reinterpret_cast<const float4*>(a.master + pos + 4);
+        const float4 p2 = *reinterpret_cast<const float4*>(a.master + pos + 8);
+        const float4 p3 = *reinterpret_cast<const float4*>(a.master + pos + 12);
+        const int tile = kk >> 4;
+        QScale qs;
+        qs.r = __uint_as_float(s_tile[tile]);
+        qs.s = __uint_as_float(s_tile[ntile + tile]);
+        qs.mode = qs.s == 0.f ? 0 : (isinf(qs.r) ? 2 : 1);
+        const float pa[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        const float pb[8] = {p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
+        const uint2 ca = codes_e4m3(pa, qs), cb = codes_e4m3(pb, qs);
+        if ((g.pos & 15) == 0) {  // the region start fixes the alignment of every pair
+          *reinterpret_cast<uint4*>(a.fp8 + pos) = make_uint4(ca.x, ca.y, cb.x, cb.y);
+        } else {
+          *reinterpret_cast<uint2*>(a.fp8 + pos) = ca;
+          *reinterpret_cast<uint2*>(a.fp8 + pos + 8) = cb;
         }
       }
       consumer_sync();  // s_tile is reused by the next region

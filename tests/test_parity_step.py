@@ -137,3 +137,24 @@ def test_dequant_view_bit_exact(cuda, name, dev):
     torch.cuda.synchronize(cuda)
     want = OF.dequant_fp8(case.olayout, case.dev_lo, case.dev_hi, codes, scales, out0)
     assert_bits_equal("bf16 view", out.cpu().numpy().view(np.uint16), want)
+
+
+@pytest.mark.parametrize("name", ["gptoss-small", "odd-start"])
+def test_start_align_8(cuda, name):
+    """Planned with 8-element starts: regions may begin 8 elements off a 16-element
+    boundary, so blocks are read directly instead of staged and the FP8 codes are
+    written in 8-byte pieces; still bit for bit.  odd-start: a 264-element vector
+    puts the next tensor's 256-column strips at 264 = 8 (mod 16)."""
+    if name == "odd-start":
+        c = W.config("llama-small")
+        tensors = [W.TensorSpec("v", 1, 264, 256, W.ADAM_FLAT256, True),
+                   W.TensorSpec("w", 256, 512, 128 * 512, W.ADAM_FLAT256, True),
+                   W.TensorSpec("u", 1, 520, 256, W.ADAM_FLAT256, False)]
+        c.start_align = 8
+        case = StepCase(c, tensors=tensors, V=1, dev_lo=0, dev_hi=1)
+        assert int(case.table.intervals[1][4]) % 16 == 8
+    else:
+        c = W.config(name)
+        c.start_align = 8
+        case = StepCase(c)
+    _compare(case, case.run_gpu(cuda), case.run_oracle())
