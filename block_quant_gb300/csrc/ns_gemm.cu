@@ -4,11 +4,14 @@
 // iteration (feynmanwiki walkthrough of veScale-FSDP, paper section 6.3).  Per
 // matrix (a tall one is iterated as its transpose):
 //   X = x / (||x||_F + eps);  repeat: A = X X^T;  B = b A + c A A;  X = a X + B X
-// Every product runs in k_gemm: bf16 operands staged by TMA into 128-byte
-// swizzled shared memory, tcgen05.mma issued by one thread into a TMEM fp32
-// accumulator, an epilogue reading TMEM with tcgen05.ld and writing
-// D = alpha*acc + beta*C in bf16.  A is symmetric, so A A is computed as A A^T
-// (both operands K-major); B X takes X as an MN-major operand.
+// Every product runs in k_gemm_p, a persistent kernel (one CTA per SM walking the
+// 128 x 256 output tiles): bf16 operands staged by TMA into 128-byte swizzled
+// shared memory, tcgen05.mma issued by one thread into one of two TMEM fp32
+// accumulators, an epilogue reading TMEM with tcgen05.ld and writing
+// D = alpha*acc + beta*C in bf16 while the next tile's products run.  A is
+// symmetric, so A A is computed as A A^T (both operands K-major), and the two
+// symmetric products run only the tiles touching the upper triangle and mirror
+// them; B X takes X as an MN-major operand.
 //
 // Every wait on an mbarrier is bounded: on timeout the kernel records an error
 // word in the workspace, drains its own copies, frees TMEM and returns.
@@ -30,7 +33,6 @@ constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr int TMEM_COLS = 256;     // one 128 x 256 fp32 accumulator
 constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
 // X X^T and (A A^T with A symmetric) have symmetric results: compute the tiles
@@ -39,6 +41,7 @@ constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
 #define BQ_NS_SYMMETRIC 1
 #endif
 constexpr int kSymmetric = BQ_NS_SYMMETRIC;
+
 
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -158,45 +161,148 @@ struct GemmArgs {
   __nv_bfloat16* D;        // output, row pitch ldd
   int64_t ldc, ldd;
   int* status;
-  int sym;  // D is symmetric (M == N): only tiles touching the upper triangle run, and mirror it
+  int sym;     // D is symmetric (M == N): only tiles touching the upper triangle run, and mirror it
+  int ntiles;  // tiles that run (symmetric: those touching the upper triangle), set by the launcher
 };
+
+// Epilogue of one 128 x 256 tile: TMEM accumulator columns [col_base, col_base +
+// 256) -> alpha * acc + beta * C -> bf16 D (symmetric results: columns >= row
+// written directly, those > row mirrored).  Called by the four epilogue warps;
+// q = the TMEM lane quarter the warp may access.
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& g, uint32_t tmem, uint32_t col_base, int m0, int n0,
+                                              int q, int lane) {
+  const int row = m0 + 32 * q + lane;
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(tmem + (uint32_t(32 * q) << 16) + col_base + uint32_t(32 * c), r);
+    const int col0 = n0 + 32 * c;
+    if (row >= g.M || col0 >= g.N) continue;
+    if (g.sym && col0 + 31 < row) continue;
+    __nv_bfloat16* drow = g.D + int64_t(row) * g.ldd;
+    const __nv_bfloat16* crow = g.C ? g.C + int64_t(row) * g.ldc : nullptr;
+    const bool cterm = crow && g.beta != 0.f;
+    const bool cvec = cterm && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(crow + col0) & 15) == 0;
+    __nv_bfloat162 o2[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      float cv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (cvec) {
+        const uint4 cw = *reinterpret_cast<const uint4*>(crow + col0 + 8 * v);
+        const __nv_bfloat162* cp = reinterpret_cast<const __nv_bfloat162*>(&cw);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(cp[j]);
+          cv[2 * j] = f.x;
+          cv[2 * j + 1] = f.y;
+        }
+      } else if (cterm) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (col0 + 8 * v + j < g.N) cv[j] = __bfloat162float(crow[col0 + 8 * v + j]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = g.alpha * __uint_as_float(r[8 * v + 2 * j]) + g.beta * cv[2 * j];
+        const float hi = g.alpha * __uint_as_float(r[8 * v + 2 * j + 1]) + g.beta * cv[2 * j + 1];
+        o2[4 * v + j] = __floats2bfloat162_rn(lo, hi);
+      }
+    }
+    const bool whole = !g.sym || col0 >= row;
+    if (whole && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(drow + col0) & 15) == 0) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint4 ow;
+        __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ow);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) op[j] = o2[4 * v + j];
+        *reinterpret_cast<uint4*>(drow + col0 + 8 * v) = ow;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int col = col0 + j;
+        if (col < g.N && (!g.sym || col >= row)) drow[col] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
+      }
+    }
+    if (g.sym) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int col = col0 + j;
+        if (col > row && col < g.N) g.D[int64_t(col) * g.ldd + row] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
+      }
+    }
+  }
+}
 
 // D[M x N] = alpha * (A[M x K] . op(B)) + beta * C.  A: K-major tensor map
 // (box 64 x 128).  B_MN = false: B given as [N x K] K-major (box 64 x 256), the
 // product is A B^T.  B_MN = true: B given as [K x N] N-contiguous (box 64 x 64,
 // four boxes per stage), the product is A B.
+// One CTA per SM walks the tiles t = blockIdx.x, + gridDim.x, ...
+// (B X: row blocks fastest; the others: column blocks fastest; symmetric results
+// skip the tiles wholly below the diagonal).  The stage ring runs on across
+// tiles, and two TMEM accumulators alternate so that the epilogue of one tile
+// overlaps the main loop of the next: the MMA warp waits for an accumulator's
+// "empty" barrier (the four epilogue warps' arrivals) before reusing it, and
+// commits its "full" barrier when the tile's products are done.
+constexpr int TMEM_COLS_P = 2 * BN;
+
+__device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// u-th tile that runs -> (m0, n0).  Full products: every tile, row blocks fastest
+// (B X) or column blocks fastest.  Symmetric results: the tiles touching the upper
+// triangle, listed row block by row block (row block bm starts at column block
+// floor(bm BM / BN)), so the CTAs share out only tiles with work.
+__device__ __forceinline__ void tile_at(int u, bool rows_first, int mt, int nt, int sym, int& m0, int& n0) {
+  if (sym) {
+    for (int bm = 0; bm < mt; ++bm) {
+      const int f = (bm * BM) / BN, cnt = nt > f ? nt - f : 0;
+      if (u < cnt) {
+        m0 = bm * BM;
+        n0 = (f + u) * BN;
+        return;
+      }
+      u -= cnt;
+    }
+    m0 = n0 = 0;  // not reached: u < the launcher's tile count
+    return;
+  }
+  const int bm = rows_first ? u % mt : u / nt, bn = rows_first ? u / mt : u % nt;
+  m0 = bm * BM;
+  n0 = bn * BN;
+}
+
 template <bool B_MN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+    k_gemm_p(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1024-byte-aligned stages
+  const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t bar_base = base + STAGES * STAGE_BYTES;
   auto full_bar = [&](int s) { return bar_base + 8u * uint32_t(s); };
   auto empty_bar = [&](int s) { return bar_base + 8u * uint32_t(STAGES + s); };
-  const uint32_t acc_bar = bar_base + 8u * uint32_t(2 * STAGES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 1));
+  auto tfull_bar = [&](int b) { return bar_base + 8u * uint32_t(2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar_base + 8u * uint32_t(2 * STAGES + 2 + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 4));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // tile order: the MN-major product (B X) runs row blocks fastest, so the CTAs
-  // resident at once share a few column blocks of X and all of B, which stay in
-  // L2; the other products run column blocks fastest
-  const int m0 = (B_MN ? blockIdx.x : blockIdx.y) * BM, n0 = (B_MN ? blockIdx.y : blockIdx.x) * BN;
+  const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN, ntiles = g.ntiles;
   const int nk = (g.K + BK - 1) / BK;
-  // symmetric output: a tile wholly below the diagonal has nothing to do (its
-  // elements are written, mirrored, by the tiles holding their transposes)
-  if (g.sym && n0 + BN <= m0) return;
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    mbar_init(acc_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);   // the MMA warp's commit
+      mbar_init(tempty_bar(b), 4);  // one arrival per epilogue warp
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), TMEM_COLS_P);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -204,122 +310,92 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
-    int issued = 0;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = uint32_t(kb / STAGES) & 1u;
-      if (!mbar_wait(empty_bar(s), ph ^ 1u, g.status, 1)) break;
-      const uint32_t a_dst = base + uint32_t(s) * STAGE_BYTES;
-      const uint32_t b_dst = a_dst + A_STAGE;
-      mbar_expect_tx(full_bar(s), STAGE_BYTES);
-      tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
-      if (B_MN) {
+    uint32_t it = 0;  // k-blocks issued over all tiles
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      int m0, n0;
+      tile_at(t, B_MN, mt, nt, g.sym, m0, n0);
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = int(it % STAGES);
+        if (!mbar_wait(empty_bar(s), ((it / STAGES) & 1u) ^ 1u, g.status, 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_dst = base + uint32_t(s) * STAGE_BYTES;
+        const uint32_t b_dst = a_dst + A_STAGE;
+        mbar_expect_tx(full_bar(s), STAGE_BYTES);
+        tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
+        if (B_MN) {
 #pragma unroll
-        for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + uint32_t(j) * (BK * 128), &tmB, n0 + 64 * j, kb * BK, full_bar(s));
-      } else {
-        tma_load_2d(b_dst, &tmB, kb * BK, n0, full_bar(s));
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(b_dst + uint32_t(j) * (BK * 128), &tmB, n0 + 64 * j, kb * BK, full_bar(s));
+        } else {
+          tma_load_2d(b_dst, &tmB, kb * BK, n0, full_bar(s));
+        }
       }
-      issued = kb + 1;
     }
     // drain: the last load issued to each stage has landed before this CTA can exit
-    for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
-      mbar_wait(full_bar(kb % STAGES), uint32_t(kb / STAGES) & 1u, g.status, 2);
+    for (uint32_t d = it > uint32_t(STAGES) ? it - STAGES : 0; d < it; ++d)
+      mbar_wait(full_bar(int(d % STAGES)), (d / STAGES) & 1u, g.status, 2);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
     constexpr uint32_t idesc = idesc_bf16(BM, BN, B_MN ? 1 : 0);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      if (!mbar_wait(full_bar(s), uint32_t(kb / STAGES) & 1u, g.status, 3)) break;
+    uint32_t it = 0, tc = 0;  // k-blocks consumed, tiles done
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      int m0, n0;
+      tile_at(t, B_MN, mt, nt, g.sym, m0, n0);
+      const int buf = int(tc & 1u);
+      if (tc >= 2 && !mbar_wait(tempty_bar(buf), ((tc >> 1) & 1u) ^ 1u, g.status, 5)) break;
       tc_fence_after();
-      const uint32_t a_addr = base + uint32_t(s) * STAGE_BYTES;
-      const uint32_t b_addr = a_addr + A_STAGE;
+      const uint32_t acc = tmem + uint32_t(buf) * BN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = int(it % STAGES);
+        if (!mbar_wait(full_bar(s), (it / STAGES) & 1u, g.status, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = base + uint32_t(s) * STAGE_BYTES;
+        const uint32_t b_addr = a_addr + A_STAGE;
 #pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk) {
-        const uint64_t ad = sdesc(a_addr + 32u * kk, 16, 1024);
-        const uint64_t bd = B_MN ? sdesc(b_addr + uint32_t(kk) * 16u * 128u, BK * 128, 1024)
-                                 : sdesc(b_addr + 32u * kk, 16, 1024);
-        mma_bf16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = sdesc(a_addr + 32u * kk, 16, 1024);
+          const uint64_t bd = B_MN ? sdesc(b_addr + uint32_t(kk) * 16u * 128u, BK * 128, 1024)
+                                   : sdesc(b_addr + 32u * kk, 16, 1024);
+          mma_bf16(acc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit(empty_bar(s));
       }
-      mma_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+      if (!ok) break;
+      mma_commit(tfull_bar(buf));
+      ++tc;
     }
-    mma_commit(acc_bar);  // accumulator complete (also after an early exit)
+    // every product issued here has finished before the accumulators are freed
+    if (tc > 0) mbar_wait(tfull_bar(int((tc - 1) & 1u)), ((tc - 1) >> 1) & 1u, g.status, 6);
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM -> registers -> alpha*acc + beta*C -> bf16
-    const int q = warp & 3;  // the TMEM lane quarter this warp may access
-    const int row = m0 + 32 * q + lane;
-    const bool ok = mbar_wait(acc_bar, 0, g.status, 4);
-    tc_fence_after();
-    if (ok) {
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(32 * c), r);
-        const int col0 = n0 + 32 * c;
-        if (row >= g.M || col0 >= g.N) continue;
-        // symmetric output: this thread writes columns >= row and mirrors those > row
-        if (g.sym && col0 + 31 < row) continue;
-        __nv_bfloat16* drow = g.D + int64_t(row) * g.ldd;
-        const __nv_bfloat16* crow = g.C ? g.C + int64_t(row) * g.ldc : nullptr;
-        const bool cterm = crow && g.beta != 0.f;
-        const bool cvec = cterm && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(crow + col0) & 15) == 0;
-        __nv_bfloat162 o2[16];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          float cv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (cvec) {
-            const uint4 cw = *reinterpret_cast<const uint4*>(crow + col0 + 8 * v);
-            const __nv_bfloat162* cp = reinterpret_cast<const __nv_bfloat162*>(&cw);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 f = __bfloat1622float2(cp[j]);
-              cv[2 * j] = f.x;
-              cv[2 * j + 1] = f.y;
-            }
-          } else if (cterm) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (col0 + 8 * v + j < g.N) cv[j] = __bfloat162float(crow[col0 + 8 * v + j]);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = g.alpha * __uint_as_float(r[8 * v + 2 * j]) + g.beta * cv[2 * j];
-            const float hi = g.alpha * __uint_as_float(r[8 * v + 2 * j + 1]) + g.beta * cv[2 * j + 1];
-            o2[4 * v + j] = __floats2bfloat162_rn(lo, hi);
-          }
-        }
-        const bool whole = !g.sym || col0 >= row;  // every column of the chunk is written directly
-        if (whole && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(drow + col0) & 15) == 0) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 ow;
-            __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ow);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) op[j] = o2[4 * v + j];
-            *reinterpret_cast<uint4*>(drow + col0 + 8 * v) = ow;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = col0 + j;
-            if (col < g.N && (!g.sym || col >= row)) drow[col] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
-          }
-        }
-        if (g.sym) {
-          // mirror: for one column the warp's lanes hold consecutive rows, so
-          // these stores are contiguous across the warp
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = col0 + j;
-            if (col > row && col < g.N) g.D[int64_t(col) * g.ldd + row] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
-          }
-        }
-      }
+    // ---------------- epilogue
+    const int q = warp & 3;
+    uint32_t tc = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      int m0, n0;
+      tile_at(t, B_MN, mt, nt, g.sym, m0, n0);
+      const int buf = int(tc & 1u);
+      const bool ok = mbar_wait(tfull_bar(buf), (tc >> 1) & 1u, g.status, 4);
+      tc_fence_after();
+      if (!ok) break;
+      epilogue_tile(g, tmem, uint32_t(buf) * BN, m0, n0, q, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(tempty_bar(buf));
+      ++tc;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, TMEM_COLS_P);
   }
 }
 
@@ -531,15 +607,22 @@ int check_mat(const bq_mat& t) {
 int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, cudaStream_t s) {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(k_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
-    cudaFuncSetAttribute(k_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    cudaFuncSetAttribute(k_gemm_p<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    cudaFuncSetAttribute(k_gemm_p<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
   });
-  const unsigned mt = unsigned((g.M + BM - 1) / BM), nt = unsigned((g.N + BN - 1) / BN);
-  const dim3 grid = b_mn ? dim3(mt, nt) : dim3(nt, mt);
+  const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN;
+  GemmArgs a = g;
+  a.ntiles = mt * nt;
+  if (g.sym) {  // the same count tile_at lists
+    a.ntiles = 0;
+    for (int bm = 0; bm < mt; ++bm) a.ntiles += std::max(0, nt - (bm * BM) / BN);
+  }
+  if (a.ntiles == 0) return BQ_OK;
+  const unsigned grid = unsigned(std::min(a.ntiles, sm_count()));
   if (b_mn)
-    k_gemm<true><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, g);
+    k_gemm_p<true><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, a);
   else
-    k_gemm<false><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, g);
+    k_gemm_p<false><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, a);
   return check("bq_muon_ns (gemm)");
 }
 
@@ -605,13 +688,13 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
     for (int it = 0; it < steps; ++it) {
       const int nxt = cur ^ 1;
       // A = X X^T
-      GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status, kSymmetric};
+      GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status, kSymmetric, 0};
       if (int rc = gemm(false, mXa[cur], mXb[cur], g1, s)) return rc;
       // B = c (A A^T) + b A   (A symmetric)
-      GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric};
+      GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric, 0};
       if (int rc = gemm(false, mAa, mAb, g2, s)) return rc;
       // X' = B X + a X
-      GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0};
+      GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0, 0};
       if (int rc = gemm(true, mBa, mXmn[cur], g3, s)) return rc;
       cur = nxt;
     }
