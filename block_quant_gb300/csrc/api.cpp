@@ -18,6 +18,19 @@ int set_error(int code, const std::string& msg) {
   return code;
 }
 
+// true the first time (device, key) is seen in this process: one-time per-device
+// set-up such as kernel attributes, which belong to the device they were set on
+bool once_per_device(int key) {
+  static std::mutex mu;
+  static bool done[64][8] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || key < 0 || key >= 8) return true;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev][key]) return false;
+  done[dev][key] = true;
+  return true;
+}
+
 int sm_count() {
   static std::mutex mu;
   static int cached[64] = {0};

@@ -605,11 +605,11 @@ int check_mat(const bq_mat& t) {
 }
 
 int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, cudaStream_t s) {
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(k_gemm_p<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
-    cudaFuncSetAttribute(k_gemm_p<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
-  });
+  if (once_per_device(kOnceGemmAttr)) {  // the attribute belongs to the current device
+    if (cudaFuncSetAttribute(k_gemm_p<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(k_gemm_p<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) != cudaSuccess)
+      return check("bq_muon_ns (gemm shared memory attribute)");
+  }
   const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN;
   GemmArgs a = g;
   a.ntiles = mt * nt;

@@ -1176,11 +1176,10 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
     const int grid = std::min(t.n_strips, sms * kStripCtas);
     const size_t smem = sizeof(TmaStage) * kRing + 2 * kRing * sizeof(uint64_t) +
                         2 * size_t(t.max_strip_tiles) * sizeof(uint32_t);
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaFuncSetAttribute(k_strip<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      cudaFuncSetAttribute(k_strip<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      attr_done = true;
+    if (once_per_device(kOnceStripAttr)) {  // the attribute belongs to the current device
+      if (cudaFuncSetAttribute(k_strip<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
+          cudaFuncSetAttribute(k_strip<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+        return check_launch("bq_step_adam8 (strip shared memory attribute)");
     }
     if (fp8)
       k_strip<true><<<grid, kStripThreads, smem, s>>>(t.strips, t.n_strips, a);
