@@ -739,13 +739,7 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {
-                "workload": f"llama3-8b-layer DBuffer step (V=8, local shards {step.lo}..{step.hi - 1})" +
-                            (" + Muon NS batch [4096x4096, 4096x14336, 14336x4096] x 5 iterations" if muon else ""),
-                "elements": step.bytes["elems"], "padding_elements": step.bytes["pads"], "S": step.table.S,
-                "bytes_per_step": B, "l2": f"inputs {step.n * 13 / 1e9:.1f} GB > L2: no flush needed",
-                "parallelism": f"dp{world}: one independent layer per GPU, no data-path collective",
-            },
+            "config": workload_config(step.bytes, step.table.S, step.lo, step.hi, step.n, bool(muon), world),
             "hbm_frac": round(value / world / pk["hbm"], 4),
             "dbuffer_ms": round(dbuf_ms_max, 4),
             "pack": {"ms": round(statistics.mean(pack_ms), 4),
@@ -854,6 +848,28 @@ def muon_launches(muon, steps=5):
     return len(muon.mats) * (4 + 3 * steps)
 
 
+def workload_config(b, S, lo, hi, n, muon, world):
+    """The config object both arms print (b: step_bytes of the benchmarked range)."""
+    return {
+        "workload": f"llama3-8b-layer DBuffer step (V=8, local shards {lo}..{hi - 1})" +
+                    (" + Muon NS batch [4096x4096, 4096x14336, 14336x4096] x 5 iterations" if muon else ""),
+        "elements": b["elems"], "padding_elements": b["pads"], "S": S,
+        "bytes_per_step": b["total"], "l2": f"inputs {n * 13 / 1e9:.1f} GB > L2: no flush needed",
+        "parallelism": f"dp{world}: one independent layer per GPU, no data-path collective",
+    }
+
+
+def reference_config(args, world):
+    """Our arm's config, with the layout figures from the oracle planner (no GPU)."""
+    from oracle import planner as OP
+
+    cfg = W.config(WORKLOAD)
+    descs = [OP.TensorDesc(t.rows, t.cols, t.g, t.adam_kind, t.fp8) for t in cfg.units[0].tensors]
+    T = W.Table(OP.plan(descs, cfg.V, cfg.alpha, cfg.start_align).export())
+    lo, hi = cfg.dev_lo, cfg.dev_lo + (args.shards or (cfg.dev_hi - cfg.dev_lo))
+    return workload_config(step_bytes(T, lo, hi), T.S, lo, hi, (hi - lo) * T.S, args.muon, world)
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle as it stands, on the host cores, same
     metric and unit, a bounded sample of the workload per step."""
@@ -872,8 +888,7 @@ def run_reference(args):
         "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
-        "config": {"workload": "llama3-8b-layer DBuffer step (V=8), bounded sample per step",
-                   "parallelism": "host, one core"},
+        "config": reference_config(args, world),
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": per_step[0]["sample"].split(":")[0] + " per step (about 1 s of CPU work)"},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
