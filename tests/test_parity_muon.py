@@ -41,3 +41,23 @@ def test_full_size_batch(cuda):
     c = W.config("muon-ns")
     errs = run_muon_case(cuda, c.muon_shapes, seed_cfg=c.cfg_id, steps=5)
     assert max(errs) < TOL, errs
+
+
+def test_degenerate_inputs(cuda):
+    """An all-zero matrix stays exactly zero (x / (0 + eps) = 0); one-row and
+    one-column matrices (rank one: every step maps the single singular value
+    through the quintic), a tiny square one and a very flat one against the fp64
+    oracle."""
+    import torch
+
+    import block_quant_gb300 as bq
+
+    x = torch.zeros(96, 160, dtype=torch.bfloat16, device=cuda)
+    y = torch.full_like(x, float("nan"))
+    mats = [(x, y, 96, 160)]
+    ws = torch.empty(bq.muon_ns_workspace(mats), dtype=torch.uint8, device=cuda)
+    bq.muon_ns(mats, ws, steps=5)
+    bq.muon_ns_check(ws)
+    assert not torch.isnan(y).any() and int(torch.count_nonzero(y)) == 0
+    errs = run_muon_case(cuda, [(1, 64), (64, 1), (8, 8), (3, 1000)], steps=5)
+    assert max(errs) < TOL, errs

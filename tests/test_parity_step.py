@@ -75,6 +75,9 @@ def _edge_tensors():
         T("tile_2d_nofp8", 129, 136, 128 * 136, W.ADAM_TILE128, False),
         T("zero_2d", 128, 256, 128 * 256, W.ADAM_FLAT256, True), # all-zero grads, params: zero scales
         T("plain_2d", 100, 24, 256 * 3, W.ADAM_FLAT256, False),
+        T("empty_1d", 1, 0, 256, W.ADAM_FLAT256, False),         # no elements at all
+        T("t32_2d", 70, 40, 32 * 40, W.ADAM_TILE32, False),      # 32x32 blocks clipped both ways
+        T("muon_2d", 96, 64, 64, W.OPT_MUON, False),             # Muon: the Adam step leaves it alone
     ]
 
 
