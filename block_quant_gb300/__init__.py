@@ -23,7 +23,7 @@ ADAM_FLAT256, ADAM_TILE128, OPT_MUON, ADAM_TILE32 = 0, 1, 2, 3
 # every entry point include/bq.h declares
 SYMBOLS = [
     "bq_strerror", "bq_last_error", "bq_version", "bq_plan", "bq_layout_free", "bq_layout_query",
-    "bq_layout_export", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_shard_check", "bq_pack",
+    "bq_layout_export", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_shard_check", "bq_wait_selftest", "bq_pack",
     "bq_step_adam8", "bq_quant_fp8", "bq_muon_ns_workspace", "bq_muon_ns", "bq_muon_ns_check",
     "bq_muon_ns_noalloc", "bq_muon_roots", "bq_muon_momentum", "bq_muon_apply", "bq_dequant_fp8",
 ]
@@ -93,6 +93,7 @@ def load():
                                P, C.c_size_t, P]
     lib.bq_muon_ns_check.argtypes = [P, C.c_size_t, P]
     lib.bq_shard_check.argtypes = [P, P]
+    lib.bq_wait_selftest.argtypes = [P, P]
     lib.bq_muon_roots.argtypes = [P, C.POINTER(C.c_int32), C.c_size_t]
     lib.bq_dequant_fp8.argtypes = [P, P, P, P, P]
     lib.bq_muon_momentum.argtypes = [P, P, P, C.c_float, P, P]
@@ -289,6 +290,12 @@ def muon_apply(shard, master, update_ptrs, lr, stream=None):
     """W <- fma(-lr[i], O_i, W) on the shard's Muon pieces (update_ptrs: int64
     device tensor of N bf16 matrix pointers, 0 = skip; lr: fp32 device tensor of N)."""
     _check(load().bq_muon_apply(shard.handle, _ptr(master), _ptr(update_ptrs), _ptr(lr), _stream(stream)))
+
+
+def wait_selftest(dev_status, stream=None):
+    """Run the bounded-wait self-test: writes 7 to dev_status (a device int32
+    tensor) once a wait that nothing completes has given up."""
+    _check(load().bq_wait_selftest(_ptr(dev_status), _stream(stream)))
 
 
 def shard_check(shard, stream=None):

@@ -271,6 +271,12 @@ int bq_muon_apply(const bq_shard* sh, float* master, const void* const* update_p
   return launch_muon_apply(sh->dev, master, reinterpret_cast<const uint16_t* const*>(update_ptrs), lr, stream);
 }
 
+int bq_wait_selftest(int* dev_status, bq_stream_t stream) {
+  if (!dev_status || (reinterpret_cast<uintptr_t>(dev_status) & 3))
+    return set_error(BQ_EINVAL, "bq_wait_selftest: dev_status NULL or misaligned");
+  return launch_wait_selftest(dev_status, stream);
+}
+
 int bq_shard_check(const bq_shard* sh, bq_stream_t stream) {
   if (!sh) return set_error(BQ_EINVAL, "bq_shard_check: shard is NULL");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

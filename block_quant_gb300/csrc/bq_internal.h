@@ -145,6 +145,7 @@ int launch_pack(const DevTables& t, const uint16_t* const* grads, uint16_t* dst,
                 int accumulate, void* stream);
 int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream);
 int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, float* fp8_scale, void* stream);
+int launch_wait_selftest(int* status, void* stream);
 int launch_dequant_fp8(const DevTables& t, const uint8_t* fp8, const float* fp8_scale, uint16_t* out, void* stream);
 int launch_muon_momentum(const DevTables& t, const uint16_t* grad, float* mom, float mu, uint16_t* const* gather,
                          void* stream);

@@ -303,8 +303,9 @@ __device__ __forceinline__ void mbar_arrive_cp_async(uint64_t* b) {
 
 constexpr long long kWaitCycles = 1LL << 31;  // about a second at the SM clock
 
-// wait for the completion of the phase of b with the given parity; false on timeout
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+// wait for the completion of the phase of b with the given parity; false once
+// `limit` SM clocks have passed
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* b, uint32_t parity, long long limit) {
   const long long t0 = clock64();
   for (;;) {
     uint32_t done;
@@ -314,9 +315,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
         : "r"(smem_u32(b)), "r"(parity)
         : "memory");
     if (done) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
 }
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) { return mbar_wait_for(b, parity, kWaitCycles); }
 
 // bulk copy global -> this CTA's shared memory, completion counted on bar
 // (addresses 16-byte aligned, bytes a multiple of 16)
@@ -1129,6 +1132,18 @@ __global__ void __launch_bounds__(kThreads) k_dequant_region(const RegionGroup* 
   }
 }
 
+// ---------------------------------------------------------------- bounded-wait self-test
+// One thread waits on an mbarrier that nothing arrives at, through the same wait
+// loop as the step kernels but with a short limit, and records code 7 when the
+// wait gives up (1 if it ever completed, which cannot happen).
+__global__ void k_wait_selftest(int* status, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  mbar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  const bool done = mbar_wait_for(&bar, 0, limit);
+  *status = done ? 1 : 7;
+}
+
 int check_launch(const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
@@ -1261,6 +1276,11 @@ int launch_dequant_fp8(const DevTables& t, const uint8_t* fp8, const float* fp8_
     if (int rc = check_launch("bq_dequant_fp8 (band tiles)")) return rc;
   }
   return BQ_OK;
+}
+
+int launch_wait_selftest(int* status, void* stream) {
+  k_wait_selftest<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(status, 1LL << 21);  // about a millisecond
+  return check_launch("bq_wait_selftest");
 }
 
 int launch_muon_momentum(const DevTables& t, const uint16_t* grad, float* mom, float mu, uint16_t* const* gather,

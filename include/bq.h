@@ -157,6 +157,14 @@ void bq_shard_free(bq_shard* shard);
  * Defined by no passage of the pages: a failure-reporting aid of this library. */
 int bq_shard_check(const bq_shard* shard, bq_stream_t stream);
 
+/* bq_wait_selftest - exercise the failure path of the kernels' bounded waits:
+ * one GPU thread waits on an mbarrier that nothing arrives at, through the same
+ * wait loop as the step kernels but with a limit of about a millisecond, gives
+ * up, writes 7 to the device int *dev_status (1 would mean the wait completed)
+ * and returns; the context stays usable.  Asynchronous on stream.  No passage of
+ * the pages defines it: a failure-detection aid of this library. */
+int bq_wait_selftest(int* dev_status, bq_stream_t stream);
+
 /* ------------------------------------------------------------------ step
  * bq_pack - group-level fused pre-communication add / scale / zero / copy.
  * Defined by: DBuffer's fused pre-communication ops (bud-325 summary, Key claims
