@@ -357,7 +357,9 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
   T.band_tiles.clear();
   T.max_strip_tiles = 0;
   constexpr int64_t kFlatGroupElems = 8192;
-  constexpr int64_t kBandPiece = 32768;  // whole 256-element blocks
+  // whole 256-element blocks; 8192 measured 4% faster than 32768 on the GPT-OSS
+  // rank-0 slice, where a layer has only a few hundred 32K pieces for 456 CTAs
+  constexpr int64_t kBandPiece = 8192;
   for (int64_t k = first; k < last; ++k) {
     const Interval& v = L.intervals[k];
     const Tensor& t = L.tensors[v.tensor];
