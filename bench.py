@@ -460,17 +460,42 @@ class ModelStep:
             bq.step_adam8(u["shard"], u["dbuf"], u["master"], u["m"], u["v"], u["ms"], u["vs"], self.hp,
                           u["fp8"], u["fs"], stream=stream)
 
+    def run_branches(self, stream, branches):
+        """The units spread round robin over side streams forked from and joined
+        back to `stream` (the units are independent), so that one unit's kernel
+        tail overlaps the next unit's kernels."""
+        torch, bq = self.torch, self.bq
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for b in branches:
+            b.wait_event(fork)
+        for i, u in enumerate(self.units):
+            b = branches[i % len(branches)]
+            bq.pack(u["shard"], u["gp"], u["dbuf"], 1.0 / u["V"], False, stream=b)
+            bq.step_adam8(u["shard"], u["dbuf"], u["master"], u["m"], u["v"], u["ms"], u["vs"], self.hp,
+                          u["fp8"], u["fs"], stream=b)
+        for b in branches:
+            join = torch.cuda.Event()
+            join.record(b)
+            stream.wait_event(join)
+
     def measure(self, stream, steps=10, warmup=3):
-        """(eager ms, graph ms) per whole-model step."""
+        """(eager ms, graph ms, 4-branch graph ms) per whole-model step."""
         torch = self.torch
         eager = time_call(lambda: self.run(stream), stream, steps, warmup)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             self.run(stream)
         replay = time_call(graph.replay, stream, steps, warmup)
-        self.bq.shard_check(self.units[0]["shard"], stream=stream)
-        del graph
-        return eager, replay
+        branches = [torch.cuda.Stream(stream.device) for _ in range(4)]
+        graph4 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph4, stream=stream):
+            self.run_branches(stream, branches)
+        replay4 = time_call(graph4.replay, stream, steps, warmup)
+        for u in self.units[:1] + self.units[-1:]:
+            self.bq.shard_check(u["shard"], stream=stream)
+        del graph, graph4
+        return eager, replay, replay4
 
 
 def time_call(fn, stream, steps, warmup):
@@ -777,13 +802,15 @@ def run_ours(args):
                 "gpt-oss-120b-rank0": "all {u} units (embedding, 36 MoE layers, head) of the rank-0 slice at V=256, "
                                       "one DBuffer each, 256-element Adam blocks + 128x128 FP8 (d = 2880: whole-band "
                                       "regions)"}
-        for mname, ((eg, gr), (mb, me, ml, mu)) in models.items():
+        for mname, ((eg, gr, gr4), (mb, me, ml, mu)) in models.items():
             line.setdefault("model_step", {})[mname] = {
                 "workload": f"{mname}: " + desc[mname].format(u=mu),
                 "elements": me, "bytes": mb, "launches": ml,
                 "eager": {"ms": round(eg, 3), "GB/s": round(mb / (eg * 1e-3) / 1e9, 1)},
                 "cuda_graph": {"ms": round(gr, 3), "GB/s": round(mb / (gr * 1e-3) / 1e9, 1),
                                "frac": round(mb / (gr * 1e-3) / 1e9 / pk["hbm"], 4)},
+                "cuda_graph_4_branches": {"ms": round(gr4, 3), "GB/s": round(mb / (gr4 * 1e-3) / 1e9, 1),
+                                          "frac": round(mb / (gr4 * 1e-3) / 1e9 / pk["hbm"], 4)},
                 "note": "measured after the timed region; not part of value",
             }
         acc_bytes = 6 * step.bytes["elems"] + 2 * step.bytes["pads"]

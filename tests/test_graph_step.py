@@ -74,3 +74,38 @@ def test_model_step_graph_replay_matches_eager(cuda):
         oa, ob = a.outputs(), b.outputs()
         for k in ("master", "m", "v", "ms", "vs", "fp8", "fs"):
             assert_bits_equal(f"{c.cfg.name} {k} (step 2)", ob[k], oa[k])
+
+
+def test_branched_graph_matches_eager(cuda):
+    """The units captured on separate branches (side streams forked from and
+    joined back to the capture stream) run concurrently in the graph and give
+    bit for bit the eager results: the units share no data."""
+    cases = [StepCase(W.config(n)) for n in ("llama-small", "llama-tile-small", "gptoss-small", "llama-tile32-small")]
+    stream = torch.cuda.Stream(cuda)
+    branches = [torch.cuda.Stream(cuda) for _ in range(3)]
+    eager = [DeviceUnit(c, cuda) for c in cases]
+    graphed = [DeviceUnit(c, cuda) for c in cases]
+    torch.cuda.synchronize(cuda)
+    with torch.cuda.stream(stream):
+        for u in eager:
+            u.step(stream)
+    torch.cuda.synchronize(cuda)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for b in branches:
+            b.wait_event(fork)
+        for i, u in enumerate(graphed):
+            u.step(branches[i % len(branches)])
+        for b in branches:
+            join = torch.cuda.Event()
+            join.record(b)
+            stream.wait_event(join)
+    g.replay()
+    torch.cuda.synchronize(cuda)
+    for c, a, b in zip(cases, eager, graphed):
+        bq.shard_check(b.shard)
+        oa, ob = a.outputs(), b.outputs()
+        for k in oa:
+            assert_bits_equal(f"{c.cfg.name} {k} (branched)", ob[k], oa[k])
