@@ -717,6 +717,24 @@ def run_ours(args):
         muon.pin_host()
         muon_e2e = muon.measure_e2e(stream)
 
+    # the toy configuration: 1.57 M parameters, L2-resident and launch-bound
+    toy = DBufferStep(W.config("toy"), dev, seed=6000 + rank)
+
+    def toy_call():
+        toy.pack(stream)
+        toy.adam(stream)
+
+    toy_eager = time_call(toy_call, stream, steps=200, warmup=20)
+    side_t = torch.cuda.Stream(dev)
+    with torch.cuda.stream(side_t):
+        gtoy = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gtoy, stream=side_t):
+            toy.pack(side_t)
+            toy.adam(side_t)
+        toy_graph = time_call(gtoy.replay, side_t, steps=200, warmup=20)
+    toy_info = (toy.bytes["total"], toy.launches)
+    del gtoy, toy
+    toy_eager, toy_graph = max_over_ranks([toy_eager, toy_graph], world, device=dev)
     models = {}
     if args.model_step:
         for mname in ("llama3-70b-rank0", "gpt-oss-120b-rank0"):
@@ -813,6 +831,15 @@ def run_ours(args):
                                           "frac": round(mb / (gr4 * 1e-3) / 1e9 / pk["hbm"], 4)},
                 "note": "measured after the timed region; not part of value",
             }
+        tb_, tl_ = toy_info
+        line["toy_step"] = {
+            "workload": "toy 2-layer d=256 unit (1.57 M parameters, V=4, all shards): pack + 8-bit Adam, "
+                        "L2-resident and launch-bound",
+            "bytes": tb_, "launches": tl_,
+            "eager": {"us": round(toy_eager * 1e3, 2), "GB/s": round(tb_ / (toy_eager * 1e-3) / 1e9, 1)},
+            "cuda_graph": {"us": round(toy_graph * 1e3, 2), "GB/s": round(tb_ / (toy_graph * 1e-3) / 1e9, 1)},
+            "note": "measured after the timed region; not part of value",
+        }
         acc_bytes = 6 * step.bytes["elems"] + 2 * step.bytes["pads"]
         line["pack_accumulate"] = {
             "workload": "llama3-8b-layer pack with accumulation into the gradient DBuffer (read grad 2 + DBuffer 2, "
