@@ -142,8 +142,10 @@ int bq_layout_export(const bq_layout* layout, int64_t* buf, size_t n);
  * copy them into the caller's device workspace dev_ws (ws_bytes, query with
  * bq_layout_upload_bytes) on stream.  *out receives a host bq_shard (free with
  * bq_shard_free) that the step calls take; the workspace must stay alive and
- * unmodified while the shard is used.  BQ_EALIGN if an interval's local offset
- * is not a multiple of 8 elements (plan with start_align % 8 == 0). */
+ * unmodified while the shard is used (besides the tables it holds the shard's
+ * device error word, read by bq_shard_check, so every shard needs its own
+ * workspace).  BQ_EALIGN if an interval's local offset is not a multiple of 8
+ * elements (plan with start_align % 8 == 0). */
 int bq_layout_upload_bytes(const bq_layout* layout, int dev_lo, int dev_hi, size_t* bytes);
 int bq_layout_upload(const bq_layout* layout, int dev_lo, int dev_hi, void* dev_ws, size_t ws_bytes,
                      bq_stream_t stream, bq_shard** out);
