@@ -30,7 +30,7 @@ SOURCES = {
     "step_kernels.cu": ["-lineinfo", "-fmad=false"],
     "ns_gemm.cu": ["-lineinfo"],
 }
-HEADERS = ["bq_internal.h"]
+HEADERS = ["bq_internal.h", "tmem_ptx.h"]
 
 
 def nvcc():

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include "bq_internal.h"
+#include "tmem_ptx.h"
 
 namespace bq {
 namespace {
@@ -506,10 +507,12 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_flat(const FlatGroup* _
 // ahead across region boundaries.  Warps 0..kCons-1 consume one block each per
 // stage: Adam, state and master written back, |p'| folded into per-column-tile
 // maxima in shared memory.  After a region's last stage they compute the tile
-// scales and convert the region's updated master to E4M3, re-reading it (this
-// CTA wrote it moments ago, so it comes from L2).  A block is staged only when
-// it is whole and starts on a 16-byte boundary of the byte arrays; any other
-// block (a band's ragged tail) is read directly from global memory.
+// scales and convert the region's updated master to E4M3: its first 64 rows
+// from a copy each warp wrote to tensor memory as it went, the other rows
+// re-read from global memory (this CTA wrote them moments ago, so they come
+// from L2).  A block is staged only when it is whole and starts on a 16-byte
+// boundary of the byte arrays; any other block (a band's ragged tail) is read
+// directly from global memory.
 
 #ifndef BQ_STRIP_CONSUMERS
 #define BQ_STRIP_CONSUMERS 8
@@ -525,6 +528,14 @@ constexpr int kRing = BQ_STRIP_RING;             // stages in the ring
 #define BQ_STRIP_CTAS_PER_SM 3
 #endif
 constexpr int kStripCtas = BQ_STRIP_CTAS_PER_SM;
+// FP8 instantiation: the updated master of a strip's first kTmemRows rows is
+// also written to tensor memory, so the FP8 pass reads it back from the SM
+// instead of L2.  Row b lives in lane quarter b % 4 (the warp that updated it:
+// b % kCons == warp and kCons % 4 == 0), columns (b / 4) * 8 .. + 7.
+constexpr int kTmemCols = 128;
+constexpr int kTmemRows = kTmemCols / 8 * 4;
+static_assert(kCons % 4 == 0, "a strip row must stay in its warp's TMEM lane quarter");
+static_assert(kStripCtas * kTmemCols <= 512, "the resident CTAs' TMEM columns fit one SM");
 
 struct TmaStage {
   uint4 g[kCons][32];   // bf16 gradients, 512 B per block
@@ -632,6 +643,8 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
   uint64_t* empty = full + kRing;
   uint32_t* s_tile = reinterpret_cast<uint32_t*>(empty + kRing);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ uint32_t s_tmem;
+  if (FP8 && warp == 0) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&full[i], 1 + kScaleLanes);  // the producer's expect_tx + one per scale lane
@@ -639,7 +652,10 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
+  if (FP8) tc_fence_before();
   __syncthreads();
+  if (FP8) tc_fence_after();
+  const uint32_t tmem = FP8 ? s_tmem + (uint32_t(32 * (warp & 3)) << 16) : 0u;  // this warp's lane quarter
   if (warp == kCons) {
     strip_producer(groups, ngroups, a, ring, full, empty, lane);
     return;
@@ -702,12 +718,18 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
         a.v_scale[slot] = qv.s;
       }
       if (fp8) {
+        if (b < kTmemRows && nb == 256) {
+          __syncwarp();  // tcgen05 loads and stores are issued by the whole warp
+          tmem_st8(tmem + uint32_t((b >> 2) * 8), o.p1);
+        }
         // a strip row: lanes 0-15 cover column tile 0, lanes 16-31 tile 1
         const uint32_t ap = __reduce_max_sync(lane < 16 ? 0x0000FFFFu : 0xFFFF0000u, o.ap);
         if ((lane & 15) == 0) atomicMax(&s_tile[lane >> 4], ap);
       }
     }
     if (fp8) {
+      __syncwarp();
+      tmem_wait_st();
       consumer_sync();
       if (!dead) {
         for (int t = threadIdx.x; t < ntile; t += kCT) {
@@ -718,10 +740,33 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
         }
       }
       consumer_sync();
-      // each thread converts two adjacent 8-element vectors of a strip row (one
-      // 128-column tile) per pass: 128 rows x 16 pairs
+      // rows held in TMEM: each warp converts the rows it updated (one 8-element
+      // vector per lane; lanes 0-15 in column tile 0, 16-31 in tile 1)
+      const int trows = dead ? 0 : min(nblk, kTmemRows);
+      for (int b = warp; b < trows; b += kCons) {
+        int64_t start;
+        int nb, slot;
+        region_block(g, b, start, nb, slot);
+        const int n = max(0, min(8, nb - lane * 8));
+        float pv[8];
+        if (nb == 256) {
+          __syncwarp();
+          tmem_ld8(tmem + uint32_t((b >> 2) * 8), pv);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) pv[i] = i < n ? a.master[start + lane * 8 + i] : 0.f;
+        }
+        const int tile = lane >> 4;
+        QScale qs;
+        qs.r = __uint_as_float(s_tile[tile]);
+        qs.s = __uint_as_float(s_tile[ntile + tile]);
+        qs.mode = qs.s == 0.f ? 0 : (isinf(qs.r) ? 2 : 1);
+        store_bytes(a.fp8 + start + lane * 8, codes_e4m3(pv, qs), n);
+      }
+      // the other rows: each thread converts two adjacent 8-element vectors of a
+      // strip row (one 128-column tile) per pass, re-reading the master from L2
       const int npair = dead ? 0 : nel >> 4;
-      for (int q = threadIdx.x; q < npair; q += kCT) {
+      for (int q = kTmemRows * 16 + threadIdx.x; q < npair; q += kCT) {
         const int r = q >> 4, kk = (q & 15) << 1;  // row, first of the two vectors
         const int64_t pos = g.pos + int64_t(r) * g.C + (kk << 3);
         const float4 p0 = *reinterpret_cast<const float4*>(a.master + pos);
@@ -744,6 +789,14 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
         }
       }
       consumer_sync();  // s_tile is reused by the next region
+    }
+  }
+  if (FP8) {  // every consumer warp is done with TMEM before it is freed
+    tc_fence_before();
+    consumer_sync();
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(s_tmem, kTmemCols);
     }
   }
 }
@@ -1192,8 +1245,11 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
     const size_t smem = sizeof(TmaStage) * kRing + 2 * kRing * sizeof(uint64_t) +
                         2 * size_t(t.max_strip_tiles) * sizeof(uint32_t);
     if (once_per_device(kOnceStripAttr)) {  // the attribute belongs to the current device
-      if (cudaFuncSetAttribute(k_strip<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
-          cudaFuncSetAttribute(k_strip<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+      // the 227 KB opt-in limit covers static and dynamic shared memory; 1 KB is
+      // left for the static part (k_strip<true> keeps its TMEM address there)
+      constexpr int kDyn = 227 * 1024 - 1024;
+      if (cudaFuncSetAttribute(k_strip<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn) != cudaSuccess ||
+          cudaFuncSetAttribute(k_strip<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn) != cudaSuccess)
         return check_launch("bq_step_adam8 (strip shared memory attribute)");
     }
     if (fp8)
