@@ -60,10 +60,13 @@ def recorded_traffic(call):
     rec = json.load(open(p)).get(call)
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
-        return None
-    return rec["traffic_bytes_per_launch"]
+    h = hashlib.sha256()  # over the kernel's sources, in the recorded order
+    for name in rec["sources"]:
+        src = os.path.join(ROOT, name)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    return rec["traffic_bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
 
 
 # ----------------------------------------------------------------------------- algorithmic bytes
