@@ -286,7 +286,8 @@ int bq_shard_check(const bq_shard* sh, bq_stream_t stream) {
   if (e == cudaSuccess && status) e = cudaMemset(sh->dev.status, 0, sizeof(int));
   if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string("bq_shard_check: ") + cudaGetErrorString(e));
   if (status)
-    return set_error(BQ_ECUDA, "bq_step_adam8: a device wait timed out (site " + std::to_string(status) + ")");
+    return set_error(BQ_ECUDA, "bq_step_adam8: device check " + std::to_string(status) +
+                                   (status == 8 ? " (a tile region larger than 128x128)" : " (a wait timed out)"));
   return BQ_OK;
 }
 

@@ -802,44 +802,95 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
 }
 
 // ---------------------------------------------------------------- 128x128 Adam tiles (+ FP8 of the same tile)
-// Phase 1: Adam, write master, block-reduce max|m'|, max v', max|p'|.
-// Phase 2: requantise m', v' (recomputed from the untouched old codes and the
-// old scales held in registers, bit-identical) and convert p' (re-read, L2).
+// Phase 1: Adam, write master, block-reduce max|m'|, max v', max|p'|; each
+// element's inputs (bf16 gradient, m code, v code) also go to tensor memory as
+// one packed 32-bit word.
+// Phase 2: requantise m', v' (recomputed bit-identically from those words and
+// the old scales held in registers) and convert p' (re-read, L2).
+// Thread t handles the tile's vectors t + 256 i (i < 8, a tile has at most 2048
+// eight-element vectors); vector i's words live in the thread's TMEM lane (lane
+// quarter warp % 4) at columns 64 (warp / 4) + 8 i .. + 7: 128 columns per CTA.
+
+constexpr int kTileTmemCols = 128;
+static_assert(kAdamCtas * kTileTmemCols <= 512, "the resident CTAs' TMEM columns fit one SM");
 
 __device__ __forceinline__ void block_max(uint32_t x, uint32_t* red, int which) {
   x = __reduce_max_sync(0xFFFFFFFFu, x);
   if ((threadIdx.x & 31) == 0) red[which * kWarps + (threadIdx.x >> 5)] = x;
 }
 
+// element e's word: bf16 gradient bits << 16 | m code << 8 | v code
+__device__ __forceinline__ void pack_inputs(const Raw8& x, uint32_t* w) {
+  const uint32_t gw[4] = {x.g.x, x.g.y, x.g.z, x.g.w};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // elements 4h .. 4h + 3
+    const uint32_t mw = h ? x.m.y : x.m.x, vw = h ? x.v.y : x.v.x;
+    const uint32_t mv01 = __byte_perm(vw, mw, 0x5140u), mv23 = __byte_perm(vw, mw, 0x7362u);  // v0 m0 v1 m1, v2 m2 v3 m3
+    w[4 * h + 0] = __byte_perm(mv01, gw[2 * h], 0x5410u);
+    w[4 * h + 1] = __byte_perm(mv01, gw[2 * h], 0x7632u);
+    w[4 * h + 2] = __byte_perm(mv23, gw[2 * h + 1], 0x5410u);
+    w[4 * h + 3] = __byte_perm(mv23, gw[2 * h + 1], 0x7632u);
+  }
+}
+
+__device__ __forceinline__ void unpack_inputs(const uint32_t* w, Raw8& x) {
+  x.g = make_uint4(__byte_perm(w[0], w[1], 0x7632u), __byte_perm(w[2], w[3], 0x7632u), __byte_perm(w[4], w[5], 0x7632u),
+                   __byte_perm(w[6], w[7], 0x7632u));
+  x.m = make_uint2(__byte_perm(__byte_perm(w[0], w[1], 0x0051u), __byte_perm(w[2], w[3], 0x0051u), 0x5410u),
+                   __byte_perm(__byte_perm(w[4], w[5], 0x0051u), __byte_perm(w[6], w[7], 0x0051u), 0x5410u));
+  x.v = make_uint2(__byte_perm(__byte_perm(w[0], w[1], 0x0040u), __byte_perm(w[2], w[3], 0x0040u), 0x5410u),
+                   __byte_perm(__byte_perm(w[4], w[5], 0x0040u), __byte_perm(w[6], w[7], 0x0040u), 0x5410u));
+}
+
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
   __shared__ uint32_t red[3 * kWarps];
+  __shared__ uint32_t s_tmem;
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) tmem_alloc(smem_u32(&s_tmem), kTileTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tcell = s_tmem + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(64 * (warp >> 2));
   const Hp h = make_hp(a.hp);
   for (int gi = ngroups - 1 - int(blockIdx.x); gi >= 0; gi -= int(gridDim.x)) {
     const RegionGroup g = groups[gi];
     const bool fp8 = FP8 && g.fslot >= 0;
     const float sm = a.m_scale[g.mslot], sv = a.v_scale[g.mslot];
     const int vpr = g.width >> 3, nvec = g.rows * vpr;
+    if (nvec > 8 * kThreads && threadIdx.x == 0) report(a.status, 8);  // not a 128x128 tile: the planner never emits one
     uint32_t am = 0, av = 0, ap = 0;
-    for (int v = threadIdx.x; v < nvec; v += 2 * kThreads) {
-      // two vectors' loads in flight per thread
-      const bool two = v + kThreads < nvec;
-      const int r0 = v / vpr, k0 = v - r0 * vpr;
+    // i advances by two (two vectors' loads in flight per thread); the loop test
+    // is warp-uniform so the whole warp issues the TMEM stores
+    for (int i = 0; i < 8 && kThreads * i + 32 * warp < nvec; i += 2) {
+      const int v0 = threadIdx.x + kThreads * i, v1 = v0 + kThreads;
+      const bool ok0 = v0 < nvec, ok1 = v1 < nvec;
+      const int r0 = v0 / vpr, k0 = v0 - r0 * vpr;
       const int64_t pos0 = g.pos + int64_t(r0) * g.C + (k0 << 3);
       int64_t pos1 = pos0;
-      if (two) {
-        const int r1 = (v + kThreads) / vpr, k1 = (v + kThreads) - r1 * vpr;
+      if (ok1) {
+        const int r1 = v1 / vpr, k1 = v1 - r1 * vpr;
         pos1 = g.pos + int64_t(r1) * g.C + (k1 << 3);
       }
-      const Raw8 x0 = raw_from_global(a, pos0, 8);
-      const Raw8 x1 = raw_from_global(a, pos1, two ? 8 : 0);
+      const Raw8 x0 = raw_from_global(a, pos0, ok0 ? 8 : 0);
+      const Raw8 x1 = raw_from_global(a, pos1, ok1 ? 8 : 0);
+      uint32_t w[8];
+      pack_inputs(x0, w);
+      __syncwarp();
+      tmem_st8(tcell + uint32_t(8 * i), w);
+      if (kThreads * (i + 1) + 32 * warp < nvec) {
+        pack_inputs(x1, w);
+        tmem_st8(tcell + uint32_t(8 * (i + 1)), w);
+      }
       Lane8 o;
-      adam_raw<true>(h, x0, 8, sm, sv, o);
-      store_p8(a.master + pos0, o.p1);
-      am = max(am, o.am);
-      av = max(av, o.av);
-      ap = max(ap, o.ap);
-      if (two) {
+      if (ok0) {
+        adam_raw<true>(h, x0, 8, sm, sv, o);
+        store_p8(a.master + pos0, o.p1);
+        am = max(am, o.am);
+        av = max(av, o.av);
+        ap = max(ap, o.ap);
+      }
+      if (ok1) {
         adam_raw<true>(h, x1, 8, sm, sv, o);
         store_p8(a.master + pos1, o.p1);
         am = max(am, o.am);
@@ -850,6 +901,8 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
     block_max(am, red, 0);
     block_max(av, red, 1);
     block_max(ap, red, 2);
+    __syncwarp();
+    tmem_wait_st();
     __syncthreads();
     uint32_t tm = 0, tv = 0, tp = 0;
 #pragma unroll
@@ -864,20 +917,36 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
       a.v_scale[g.mslot] = qv.s;
       if (fp8) a.fp8_scale[g.fslot] = qp.s;
     }
-    for (int v = threadIdx.x; v < nvec; v += kThreads) {
-      const int r = v / vpr, k = v - r * vpr;
-      const int64_t pos = g.pos + int64_t(r) * g.C + (k << 3);
-      const Raw8 x = raw_from_global(a, pos, 8);  // old codes; the master words now hold p'
-      Lane8 o;
-      adam_raw<true>(h, x, 8, sm, sv, o);
-      *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);
-      *reinterpret_cast<uint2*>(a.v + pos) = codes_uint8(o.v1, qv);
-      if (fp8) {
-        const float pv[8] = {x.p0.x, x.p0.y, x.p0.z, x.p0.w, x.p1.x, x.p1.y, x.p1.z, x.p1.w};
-        *reinterpret_cast<uint2*>(a.fp8 + pos) = codes_e4m3(pv, qp);
+    for (int i = 0; i < 8 && kThreads * i + 32 * warp < nvec; ++i) {
+      uint32_t w[8];
+      __syncwarp();
+      tmem_ld8(tcell + uint32_t(8 * i), w);
+      const int v = threadIdx.x + kThreads * i;
+      if (v < nvec) {
+        const int r = v / vpr, k = v - r * vpr;
+        const int64_t pos = g.pos + int64_t(r) * g.C + (k << 3);
+        Raw8 x;
+        unpack_inputs(w, x);
+        x.p0 = x.p1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        Lane8 o;
+        adam_raw<true>(h, x, 8, sm, sv, o);
+        *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);
+        *reinterpret_cast<uint2*>(a.v + pos) = codes_uint8(o.v1, qv);
+        if (fp8) {  // the master words now hold p'
+          const float4 p0 = *reinterpret_cast<const float4*>(a.master + pos);
+          const float4 p1 = *reinterpret_cast<const float4*>(a.master + pos + 4);
+          const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          *reinterpret_cast<uint2*>(a.fp8 + pos) = codes_e4m3(pv, qp);
+        }
       }
     }
     __syncthreads();  // red is reused by the next tile
+  }
+  tc_fence_before();
+  __syncthreads();  // every warp is done with TMEM before it is freed
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(s_tmem, kTileTmemCols);
   }
 }
 

@@ -154,8 +154,10 @@ void bq_shard_free(bq_shard* shard);
 /* bq_shard_check - synchronise `stream` and read the shard's device error word
  * (kept in its workspace): the 2-D Adam kernel's producer / consumer waits give
  * up after about a second, record where (1, 2: the copy producer; 3: a compute
- * warp) and let the kernel exit.  BQ_OK if no wait timed out since the last
- * check (the word is then cleared), BQ_ECUDA otherwise or on a CUDA error.
+ * warp) and let the kernel exit; 8 records a 128x128-tile region larger than a
+ * tile (a corrupted table: its excess is not updated).  BQ_OK if the word is
+ * clear; otherwise the word is cleared and BQ_ECUDA returned (also on a CUDA
+ * error).
  * Defined by no passage of the pages: a failure-reporting aid of this library. */
 int bq_shard_check(const bq_shard* shard, bq_stream_t stream);
 
