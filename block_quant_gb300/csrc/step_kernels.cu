@@ -955,13 +955,25 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
 // 6.3): 32x32 blocks of the 2-D view, kept whole on one device by a 32-row
 // granularity.  A group is a 32-row band x <= 256 columns; warp w takes the
 // group's tile w (1..4 eight-element vectors per row).  Phase 1: Adam over the
-// tile, p' written, max|m'| and max v' reduced over the warp.  Phase 2: m' and v'
-// recomputed bit-identically from the untouched old codes (the warp read them
-// moments ago, so the loads hit L1 / L2) and requantised.
+// tile, p' written, max|m'| and max v' reduced over the warp; each element's
+// inputs (bf16 gradient, m code, v code) also go to tensor memory as one packed
+// word.  Phase 2: m' and v' recomputed bit-identically from those words and
+// requantised.  Lane l handles the tile's vectors l + 32 i (i < 4); vector i's
+// words live in the lane's TMEM row (lane quarter warp % 4) at columns
+// 32 (warp / 4) + 8 i .. + 7: 64 columns per CTA.
+
+constexpr int kTile32TmemCols = 64;
+static_assert(kAdamCtas * kTile32TmemCols <= 512, "the resident CTAs' TMEM columns fit one SM");
 
 __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGroup* __restrict__ groups, int ngroups,
                                                               AdamArgs a) {
+  __shared__ uint32_t s_tmem;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) tmem_alloc(smem_u32(&s_tmem), kTile32TmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tcell = s_tmem + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(32 * (warp >> 2));
   const Hp h = make_hp(a.hp);
   for (int gi = ngroups - 1 - int(blockIdx.x); gi >= 0; gi -= int(gridDim.x)) {
     const RegionGroup g = groups[gi];
@@ -969,6 +981,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGrou
     if (c >= g.width) continue;  // warp-uniform
     const int vpr = min(32, g.width - c) >> 3;
     const int nvec = g.rows * vpr;
+    if (nvec > 128 && lane == 0) report(a.status, 8);  // not a 32x32 tile: the planner never emits one
     const int slot = g.mslot + warp;
     const float sm = a.m_scale[slot], sv = a.v_scale[slot];
     auto vpos = [&](int v) {
@@ -976,17 +989,28 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGrou
       return g.pos + int64_t(r) * g.C + c + (k << 3);
     };
     uint32_t am = 0, av = 0;
-    for (int v = lane; v < nvec; v += 64) {
-      const bool two = v + 32 < nvec;
-      const int64_t p0 = vpos(v), p1 = two ? vpos(v + 32) : p0;
-      const Raw8 x0 = raw_from_global(a, p0, 8);
-      const Raw8 x1 = raw_from_global(a, p1, two ? 8 : 0);
+    for (int i = 0; i < 4 && 32 * i < nvec; i += 2) {  // two vectors' loads in flight per lane
+      const int v0 = lane + 32 * i, v1 = v0 + 32;
+      const bool ok0 = v0 < nvec, ok1 = v1 < nvec;
+      const int64_t p0 = ok0 ? vpos(v0) : g.pos, p1 = ok1 ? vpos(v1) : g.pos;
+      const Raw8 x0 = raw_from_global(a, p0, ok0 ? 8 : 0);
+      const Raw8 x1 = raw_from_global(a, p1, ok1 ? 8 : 0);
+      uint32_t w[8];
+      pack_inputs(x0, w);
+      __syncwarp();  // tcgen05 loads and stores are issued by the whole warp
+      tmem_st8(tcell + uint32_t(8 * i), w);
+      if (32 * (i + 1) < nvec) {
+        pack_inputs(x1, w);
+        tmem_st8(tcell + uint32_t(8 * (i + 1)), w);
+      }
       Lane8 o;
-      adam_raw<true>(h, x0, 8, sm, sv, o);
-      store_p8(a.master + p0, o.p1);
-      am = max(am, o.am);
-      av = max(av, o.av);
-      if (two) {
+      if (ok0) {
+        adam_raw<true>(h, x0, 8, sm, sv, o);
+        store_p8(a.master + p0, o.p1);
+        am = max(am, o.am);
+        av = max(av, o.av);
+      }
+      if (ok1) {
         adam_raw<true>(h, x1, 8, sm, sv, o);
         store_p8(a.master + p1, o.p1);
         am = max(am, o.am);
@@ -999,18 +1023,30 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGrou
       a.m_scale[slot] = qm.s;
       a.v_scale[slot] = qv.s;
     }
-    for (int v = lane; v < nvec; v += 32) {
-      const int64_t pos = vpos(v);
-      Raw8 x;
-      x.g = *reinterpret_cast<const uint4*>(a.grad + pos);
-      x.m = *reinterpret_cast<const uint2*>(a.m + pos);
-      x.v = *reinterpret_cast<const uint2*>(a.v + pos);
-      x.p0 = x.p1 = make_float4(0.f, 0.f, 0.f, 0.f);
-      Lane8 o;
-      adam_raw<true>(h, x, 8, sm, sv, o);
-      *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);
-      *reinterpret_cast<uint2*>(a.v + pos) = codes_uint8(o.v1, qv);
+    __syncwarp();
+    tmem_wait_st();
+    for (int i = 0; i < 4 && 32 * i < nvec; ++i) {
+      uint32_t w[8];
+      __syncwarp();
+      tmem_ld8(tcell + uint32_t(8 * i), w);
+      const int v = lane + 32 * i;
+      if (v < nvec) {
+        const int64_t pos = vpos(v);
+        Raw8 x;
+        unpack_inputs(w, x);
+        x.p0 = x.p1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        Lane8 o;
+        adam_raw<true>(h, x, 8, sm, sv, o);
+        *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);
+        *reinterpret_cast<uint2*>(a.v + pos) = codes_uint8(o.v1, qv);
+      }
     }
+  }
+  tc_fence_before();
+  __syncthreads();  // every warp is done with TMEM before it is freed
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(s_tmem, kTile32TmemCols);
   }
 }
 
