@@ -44,10 +44,21 @@ def test_step_matches_oracle(cuda, name, dev):
     _compare(case, case.run_gpu(cuda), case.run_oracle())
 
 
-def test_step_without_fp8_output(cuda):
-    case = StepCase(W.config("llama-small"))
+@pytest.mark.parametrize("name", ["llama-small", "llama-tile-small", "llama-tile32-small", "gptoss-small"])
+def test_step_without_fp8_output(cuda, name):
+    """fp8_out = NULL: the kernels' no-FP8 instantiations (strips, 128x128 and
+    32x32 tiles, band pieces) leave every FP8 output alone and update the rest
+    exactly as the oracle does."""
+    case = StepCase(W.config(name))
     got = case.run_gpu(cuda, fp8=False)
     _compare(case, got, case.run_oracle(), fp8=False)
+
+
+def test_edge_shapes_without_fp8_output(cuda):
+    c = W.config("toy")
+    c.cfg_id = 42
+    case = StepCase(c, tensors=_edge_tensors(), V=3, dev_lo=0, dev_hi=3)
+    _compare(case, case.run_gpu(cuda, fp8=False), case.run_oracle(), fp8=False)
 
 
 def test_pack_accumulate_and_scale(cuda):
