@@ -52,21 +52,40 @@ def peaks():
 def recorded_traffic(call):
     """DRAM bytes per launch of `call` from the committed ncu record, or None when
     the kernel source changed since the counters were taken."""
-    import hashlib
-
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(call)
     if not rec:
         return None
-    h = hashlib.sha256()  # over the kernel's sources, in the recorded order
-    for name in rec["sources"]:
-        src = os.path.join(ROOT, name)
-        if not os.path.exists(src):
-            return None
-        h.update(open(src, "rb").read())
-    return rec["traffic_bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
+    paths = [os.path.join(ROOT, name) for name in rec["sources"]]
+    if not all(os.path.exists(q) for q in paths):
+        return None
+    return rec["traffic_bytes_per_launch"] if code_digest(paths) == rec["code_sha256"] else None
+
+
+def code_digest(paths):
+    """sha256 over C/C++/CUDA sources with comments and blank lines removed, so
+    that the record follows the code, not its commentary."""
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for q in paths:
+        text = re.sub(r"/\*.*?\*/", "", open(q).read(), flags=re.S)
+        for line in text.splitlines():
+            # a // comment: the first // that is not inside a string literal
+            out, quoted = [], False
+            for i, ch in enumerate(line):
+                if ch == '"' and (i == 0 or line[i - 1] != "\\"):
+                    quoted = not quoted
+                if not quoted and line.startswith("//", i):
+                    break
+                out.append(ch)
+            code = "".join(out).rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()
 
 
 # ----------------------------------------------------------------------------- algorithmic bytes

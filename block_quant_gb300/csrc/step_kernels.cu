@@ -6,9 +6,13 @@
 //                  optionally fused with 1x128 FP8 tiles of 1-D tensors
 //   k_strip<FP8>   8-bit Adam with flat 256-element blocks over a 2-D region,
 //                  fused with 128x128 FP8 tiles; inputs staged by a producer
-//                  warp's bulk (TMA) copies, tile amax in shared memory
-//   k_tile<FP8>    8-bit Adam with 128x128 state tiles (+ FP8 of the same tile)
-//   k_tile32       8-bit Adam with the pages' 32x32 state tiles
+//                  warp's bulk (TMA) copies, tile amax in shared memory, half
+//                  of each region's updated master kept in tensor memory for
+//                  the FP8 pass
+//   k_tile<FP8>    8-bit Adam with 128x128 state tiles (+ FP8 of the same tile);
+//                  the tile's inputs kept in tensor memory between its phases
+//   k_tile32       8-bit Adam with the walkthrough's 32x32 state tiles (same
+//                  tensor-memory scheme)
 //   k_quant_*      standalone FP8 requantisation
 //   k_dequant_*    the bf16 view (code x tile scale) of the gathered FP8 buffer
 //   k_muon_*       Muon's momentum + gather and apply around Newton-Schulz
