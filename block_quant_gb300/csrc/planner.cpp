@@ -357,6 +357,10 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
   T.band_tiles.clear();
   T.max_strip_tiles = 0;
   constexpr int64_t kFlatGroupElems = 8192;
+  // 1-D tensors (norms, biases: small) go in groups of one block per warp, so
+  // their few blocks spread over many CTAs instead of one CTA looping over them
+  // (a 1-D Llama-3-70B norm took 13 us as one 8192-element group)
+  auto flat_group = [&](const Tensor& t, int64_t block) { return t.one_d() ? 8 * block : kFlatGroupElems; };
   // whole 256-element blocks; 8192 measured 4% faster than 32768 on the GPT-OSS
   // rank-0 slice, where a layer has only a few hundred 32K pieces for 456 CTAs
   constexpr int64_t kBandPiece = 8192;
@@ -375,9 +379,9 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
     }
     if (t.adam_kind == BQ_ADAM_TILE32) {
       if (t.one_d()) {
-        for (int64_t off = 0; off < v.len; off += kFlatGroupElems)
-          T.flat32.push_back(FlatGroup{pos0 + off, int32_t(std::min(kFlatGroupElems, v.len - off)),
-                                       int32_t(mslot + off / 32), -1, 0});
+        const int64_t gs = flat_group(t, 32);
+        for (int64_t off = 0; off < v.len; off += gs)
+          T.flat32.push_back(FlatGroup{pos0 + off, int32_t(std::min(gs, v.len - off)), int32_t(mslot + off / 32), -1, 0});
       } else {
         // 32-row bands x 256-column chunks: 8 tiles per group, one warp each
         const int64_t C = t.cols;
@@ -395,14 +399,16 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
       continue;
     }
     if (t.adam_kind == BQ_ADAM_FLAT256 && (t.one_d() || !t.fp8)) {
-      for (int64_t off = 0; off < v.len; off += kFlatGroupElems) {
-        const int64_t n = std::min(kFlatGroupElems, v.len - off);
+      const int64_t gs = flat_group(t, 256);
+      for (int64_t off = 0; off < v.len; off += gs) {
+        const int64_t n = std::min(gs, v.len - off);
         T.flat256.push_back(FlatGroup{pos0 + off, int32_t(n), int32_t(mslot + off / 256),
                                       fslot < 0 ? -1 : int32_t(fslot + off / 128), 0});
       }
     } else if (t.adam_kind == BQ_ADAM_TILE128 && t.one_d()) {
-      for (int64_t off = 0; off < v.len; off += kFlatGroupElems) {
-        const int64_t n = std::min(kFlatGroupElems, v.len - off);
+      const int64_t gs = flat_group(t, 128);
+      for (int64_t off = 0; off < v.len; off += gs) {
+        const int64_t n = std::min(gs, v.len - off);
         T.flat128.push_back(FlatGroup{pos0 + off, int32_t(n), int32_t(mslot + off / 128),
                                       fslot < 0 ? -1 : int32_t(fslot + off / 128), 0});
       }
