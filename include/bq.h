@@ -202,7 +202,11 @@ int bq_pack(const bq_shard* shard, const void* const* grad_ptrs, void* dbuf_grad
  * grad: bf16 packed buffer; master fp32, m int8, v uint8, fp8_out uint8 - all
  * (dev_hi-dev_lo)*S elements, updated in place (padding untouched); m_scale,
  * v_scale: fp32 per Adam slot; fp8_scale: fp32 per FP8 slot (a scale buffer may
- * be NULL when the range has no slot of its kind).  hp: host pointer. */
+ * be NULL when the range has no slot of its kind).  hp: host pointer.
+ * Resources: the 2-D kernels take 64 or 128 tensor-memory columns per CTA for
+ * their lifetime (at most 384 of an SM's 512); a CTA whose columns are held by
+ * a co-resident kernel (e.g. a tensor-core GEMM on another stream) waits until
+ * that kernel's CTA exits. */
 int bq_step_adam8(const bq_shard* shard, const void* grad, float* master, int8_t* m, uint8_t* v, float* m_scale,
                   float* v_scale, const bq_adam_hp* hp, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream);
 
