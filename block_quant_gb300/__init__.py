@@ -23,7 +23,7 @@ ADAM_FLAT256, ADAM_TILE128, OPT_MUON, ADAM_TILE32 = 0, 1, 2, 3
 # every entry point include/bq.h declares
 SYMBOLS = [
     "bq_strerror", "bq_last_error", "bq_version", "bq_plan", "bq_layout_free", "bq_layout_query",
-    "bq_layout_export", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_shard_check", "bq_wait_selftest", "bq_pack",
+    "bq_layout_export", "bq_adam_hparams", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_shard_check", "bq_wait_selftest", "bq_pack",
     "bq_step_adam8", "bq_quant_fp8", "bq_muon_ns_workspace", "bq_muon_ns", "bq_muon_ns_check",
     "bq_muon_ns_noalloc", "bq_muon_roots", "bq_muon_momentum", "bq_muon_apply", "bq_dequant_fp8",
 ]
@@ -81,6 +81,7 @@ def load():
     lib.bq_layout_free.restype = None
     lib.bq_layout_query.argtypes = [P, C.POINTER(LayoutInfo)]
     lib.bq_layout_export.argtypes = [P, C.POINTER(C.c_int64), C.c_size_t]
+    lib.bq_adam_hparams.argtypes = [C.c_double, C.c_double, C.c_double, C.c_double, C.c_int64, C.POINTER(AdamHp)]
     lib.bq_layout_upload_bytes.argtypes = [P, C.c_int, C.c_int, C.POINTER(C.c_size_t)]
     lib.bq_layout_upload.argtypes = [P, C.c_int, C.c_int, P, C.c_size_t, P, C.POINTER(P)]
     lib.bq_shard_free.argtypes = [P]
@@ -216,10 +217,11 @@ def plan(descs, V, alpha=128, start_align=16, order=ORDER_GIVEN):
 
 
 def adam_hparams(lr, b1, b2, eps, t):
-    """fp32 hyper-parameters; the derived ones (1-b1, 1-b2 and the reciprocal bias
-    corrections 1/(1-b^t)) in fp64, rounded once."""
-    lr, b1, b2, eps = float(lr), float(b1), float(b2), float(eps)
-    return AdamHp(lr, b1, b2, eps, 1.0 - b1, 1.0 - b2, 1.0 / (1.0 - b1 ** t), 1.0 / (1.0 - b2 ** t))
+    """The library's bq_adam_hp for step t (bq_adam_hparams derives 1-b and the
+    bias corrections)."""
+    hp = AdamHp()
+    _check(load().bq_adam_hparams(float(lr), float(b1), float(b2), float(eps), int(t), C.byref(hp)))
+    return hp
 
 
 def pack(shard, grad_ptrs, dbuf_grad, scale, accumulate=False, stream=None):
@@ -306,8 +308,11 @@ def shard_check(shard, stream=None):
 
 def muon_ns_check(ws, ws_bytes=None, stream=None):
     """Synchronise the stream and raise if a device wait of the last muon_ns on
-    this workspace timed out."""
-    if ws_bytes is None:
+    this workspace timed out; ws = None: the last muon_ns_noalloc on the current
+    device (its static scratch)."""
+    if ws is None:
+        ws_bytes = 0
+    elif ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size()
     _check(load().bq_muon_ns_check(_ptr(ws), int(ws_bytes), _stream(stream)))
 
@@ -315,7 +320,8 @@ def muon_ns_check(ws, ws_bytes=None, stream=None):
 def muon_ns_noalloc(mats, steps=5, a=3.4445, b=-4.7750, c=2.0315, eps=1e-7, stream=None):
     """Newton-Schulz for callers that cannot allocate device memory: the library
     uses its own fixed 32 MiB device scratch (shared by all calls; order calls
-    that could overlap).  Batches needing more scratch raise BQ_ENOSPC."""
+    that could overlap).  Batches needing more scratch raise BQ_ENOSPC; read the
+    call's device error word with muon_ns_check(None)."""
     arr = _mats(mats)
     _check(load().bq_muon_ns_noalloc(len(arr), arr, int(steps), float(a), float(b), float(c), float(eps),
                                      _stream(stream)))

@@ -3,6 +3,7 @@
 // checks arguments, builds integer work tables and launches.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -236,6 +237,20 @@ int bq_step_adam8(const bq_shard* sh, const void* grad, float* master, int8_t* m
   AdamArgs a{static_cast<const uint16_t*>(grad), master, m, v, m_scale, v_scale, fp8_out, fp8_scale, *hp,
              sh->dev.status};
   return launch_adam8(sh->dev, a, stream);
+}
+
+int bq_adam_hparams(double lr, double b1, double b2, double eps, int64_t t, bq_adam_hp* out) {
+  if (!out) return set_error(BQ_EINVAL, "bq_adam_hparams: out is NULL");
+  if (t < 1) return set_error(BQ_EINVAL, "bq_adam_hparams: the step count t starts at 1");
+  if (!(b1 >= 0.0 && b1 < 1.0) || !(b2 >= 0.0 && b2 < 1.0))
+    return set_error(BQ_EINVAL, "bq_adam_hparams: b1 and b2 must lie in [0, 1)");
+  if (!(lr >= 0.0) || !std::isfinite(lr) || !(eps >= 0.0) || !std::isfinite(eps))
+    return set_error(BQ_EINVAL, "bq_adam_hparams: lr and eps must be finite and non-negative");
+  // fp64 throughout, one rounding to fp32 at the end
+  const double bc1 = 1.0 - std::pow(b1, double(t)), bc2 = 1.0 - std::pow(b2, double(t));
+  *out = bq_adam_hp{float(lr), float(b1), float(b2), float(eps), float(1.0 - b1), float(1.0 - b2),
+                    float(1.0 / bc1), float(1.0 / bc2)};
+  return BQ_OK;
 }
 
 int bq_quant_fp8(const bq_shard* sh, const float* master, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream) {

@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // ---------------------------------------------------------------- normalisation and copies
 
 constexpr int kRedThreads = 256, kRedBlocks = 1024;
+constexpr size_t kStatusOffset = kRedBlocks * sizeof(float);  // device error word in every workspace
 
 // partial sums of x^2 (fp32) per block, x: rows x cols bf16 with pitch ld;
 // blocks stride over rows, threads over columns
@@ -551,7 +552,7 @@ NsPlan ns_plan(const bq_mat& t) {
   size_t o = 0;
   p.off_part = o;
   o += kRedBlocks * sizeof(float);
-  p.off_status = o;
+  p.off_status = o;  // == kStatusOffset for every matrix
   o += 256;
   p.off_x0 = o;
   o += size_t(p.m) * p.ldx * 2;
@@ -619,11 +620,20 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
   if (batch > 0 && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)))
     return set_error(BQ_EALIGN, "bq_muon_ns: workspace must be 256-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // every matrix is checked before any work is queued
+  for (int i = 0; i < batch; ++i) {
+    if (int rc = check_mat(mats[i])) return rc;
+    if (ws_bytes < ns_plan(mats[i]).bytes) return set_error(BQ_ENOSPC, "bq_muon_ns: workspace too small");
+  }
+  // the device error word sits at the same offset for every matrix; it is
+  // cleared once per call, so a wait that gave up on any matrix of the batch
+  // stays recorded (report() keeps the first site) until the next call
+  if (batch > 0 &&
+      cudaMemsetAsync(static_cast<unsigned char*>(ws) + kStatusOffset, 0, sizeof(int), s) != cudaSuccess)
+    return check("bq_muon_ns (status)");
   for (int i = 0; i < batch; ++i) {
     const bq_mat& t = mats[i];
-    if (int rc = check_mat(t)) return rc;
     const NsPlan p = ns_plan(t);
-    if (ws_bytes < p.bytes) return set_error(BQ_ENOSPC, "bq_muon_ns: workspace too small");
     auto* w = static_cast<unsigned char*>(ws);
     float* part = reinterpret_cast<float*>(w + p.off_part);
     int* status = reinterpret_cast<int*>(w + p.off_status);
@@ -635,8 +645,6 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
     const auto* x = static_cast<const __nv_bfloat16*>(t.x);
     auto* y = static_cast<__nv_bfloat16*>(t.y);
 
-    // the device error word starts clear for every matrix
-    if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return check("bq_muon_ns (status)");
     // normalise into X0 (transposed for a tall input)
     k_sumsq<<<kRedBlocks, kRedThreads, 0, s>>>(x, t.rows, t.cols, t.ld_x, part);
     if (int rc = check("bq_muon_ns (norm)")) return rc;
@@ -690,27 +698,32 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_ns_scratch[kStaticScratchBytes];
 
-int muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* stream) {
-  // The array's device address, looked up once per device with that device
-  // current (in host code the symbol is only a stand-in, not a device address).
+// The array's device address on the current device, looked up once per device
+// with that device current (in host code the symbol is only a stand-in, not a
+// device address).  The cache is never refreshed: after cudaDeviceReset the
+// address may be stale.
+int static_scratch(void** out) {
   static std::mutex mu;
   static void* addr[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
     return set_error(BQ_EDEVICE, "bq_muon_ns_noalloc: no usable current device");
-  void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-      void* p = nullptr;
-      const cudaError_t e = cudaGetSymbolAddress(&p, g_ns_scratch);
-      if (e != cudaSuccess || !p)
-        return set_error(BQ_ECUDA, std::string("bq_muon_ns_noalloc: scratch address lookup failed: ") +
-                                       cudaGetErrorString(e));
-      addr[dev] = p;
-    }
-    scratch = addr[dev];
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_ns_scratch);
+    if (e != cudaSuccess || !p)
+      return set_error(BQ_ECUDA, std::string("bq_muon_ns_noalloc: scratch address lookup failed: ") +
+                                     cudaGetErrorString(e));
+    addr[dev] = p;
   }
+  *out = addr[dev];
+  return BQ_OK;
+}
+
+int muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* stream) {
+  void* scratch = nullptr;
+  if (int rc = static_scratch(&scratch)) return rc;
   size_t need = 0;
   if (int rc = muon_ns_workspace(batch, mats, &need)) return rc;
   if (need > kStaticScratchBytes)
@@ -720,14 +733,20 @@ int muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, 
   return muon_ns(batch, mats, steps, a, b, c, eps, scratch, kStaticScratchBytes, stream);
 }
 
+// ws == NULL: the static scratch of the current device (bq_muon_ns_noalloc)
 int muon_ns_check(const void* ws, size_t ws_bytes, void* stream) {
-  if (!ws || ws_bytes < kRedBlocks * sizeof(float) + sizeof(int)) return set_error(BQ_EINVAL, "bq_muon_ns_check: bad workspace");
+  if (!ws) {
+    void* scratch = nullptr;
+    if (int rc = static_scratch(&scratch)) return rc;
+    ws = scratch;
+    ws_bytes = kStaticScratchBytes;
+  }
+  if (ws_bytes < kStatusOffset + sizeof(int)) return set_error(BQ_EINVAL, "bq_muon_ns_check: bad workspace");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int status = 0;
   cudaError_t e = cudaStreamSynchronize(s);
   if (e == cudaSuccess)
-    e = cudaMemcpy(&status, static_cast<const unsigned char*>(ws) + kRedBlocks * sizeof(float), sizeof(int),
-                   cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(&status, static_cast<const unsigned char*>(ws) + kStatusOffset, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string("bq_muon_ns_check: ") + cudaGetErrorString(e));
   if (status) return set_error(BQ_ECUDA, "bq_muon_ns: a device wait timed out (site " + std::to_string(status) + ")");
   return BQ_OK;

@@ -89,9 +89,9 @@ typedef struct {
   int64_t case3_prefix;  /* length of the winning Case-3 prefix */
 } bq_layout_info;
 
-/* fp32 Adam hyper-parameters; omb1 = 1-b1, omb2 = 1-b2 and the reciprocal bias
- * corrections rbc1 = 1/(1-b1^t), rbc2 = 1/(1-b2^t) are supplied by the caller
- * (computed in fp64, rounded once to fp32). */
+/* fp32 Adam hyper-parameters of one step; omb1 = 1-b1, omb2 = 1-b2 and the
+ * reciprocal bias corrections rbc1 = 1/(1-b1^t), rbc2 = 1/(1-b2^t).  Fill it
+ * with bq_adam_hparams. */
 typedef struct {
   float lr, b1, b2, eps, omb1, omb2, rbc1, rbc2;
 } bq_adam_hp;
@@ -210,6 +210,16 @@ int bq_pack(const bq_shard* shard, const void* const* grad_ptrs, void* dbuf_grad
 int bq_step_adam8(const bq_shard* shard, const void* grad, float* master, int8_t* m, uint8_t* v, float* m_scale,
                   float* v_scale, const bq_adam_hp* hp, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream);
 
+/* bq_adam_hparams - the hyper-parameters of step t (t >= 1) of bq_step_adam8.
+ * Defined by: Adam's bias-corrected moment estimates (the 8-bit Adam of the
+ * feynmanwiki walkthrough, paper section 6.3, keeps Adam's update and quantises
+ * only the state).  lr, b1, b2, eps are taken as given (double) and rounded once
+ * to fp32; omb1 = 1-b1, omb2 = 1-b2, rbc1 = 1/(1-b1^t), rbc2 = 1/(1-b2^t) are
+ * evaluated in fp64 (b^t by the C library's pow) and rounded once to fp32.
+ * Host only; out: caller's struct.  BQ_EINVAL: out NULL, t < 1, b1 or b2 outside
+ * [0, 1), or a non-finite / negative lr or eps. */
+int bq_adam_hparams(double lr, double b1, double b2, double eps, int64_t t, bq_adam_hp* out);
+
 /* bq_quant_fp8 - standalone FP8 requantisation of master into fp8_out / fp8_scale
  * (same tile rule as above). */
 int bq_quant_fp8(const bq_shard* shard, const float* master, uint8_t* fp8_out, float* fp8_scale,
@@ -234,9 +244,12 @@ int bq_muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float
 
 /* bq_muon_ns_check - synchronise `stream` and read the workspace's device error
  * word: every wait inside the tensor-core kernels gives up after about two
- * seconds, records where, and lets the kernel exit cleanly.  BQ_OK if no wait
- * timed out during the last bq_muon_ns on this workspace, BQ_ECUDA otherwise
- * (or on a CUDA error). */
+ * seconds, records where, and lets the kernel exit cleanly.  The word is
+ * cleared once at the start of each bq_muon_ns call and keeps the first site
+ * recorded for any matrix of that call's batch.  BQ_OK if no wait timed out
+ * during the last bq_muon_ns on this workspace, BQ_ECUDA otherwise (or on a
+ * CUDA error).  ws == NULL reads the static scratch of the current device
+ * instead, i.e. the word of the last bq_muon_ns_noalloc call on it. */
 int bq_muon_ns_check(const void* ws, size_t ws_bytes, bq_stream_t stream);
 
 /* bq_dequant_fp8 - the bf16 view of the FP8 buffer after the AllGather.
@@ -311,8 +324,10 @@ int bq_muon_apply(const bq_shard* shard, float* master, const void* const* updat
  * with that device current; make that first call before any stream capture.
  * All calls share the one array and each call overwrites it: calls that can
  * overlap on the GPU (different streams without ordering between them) race,
- * so order them.  The device error word lives in the shared scratch and cannot
- * be read through bq_muon_ns_check. */
+ * so order them.  The device error word lives in the shared scratch too: read
+ * it with bq_muon_ns_check(NULL, 0, stream) after the call (same device
+ * current).  The address looked up on the first call is kept for the process;
+ * after a cudaDeviceReset it may be stale. */
 int bq_muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps,
                        bq_stream_t stream);
 

@@ -233,3 +233,22 @@ def test_placement_orders_match_oracle(built):
             assert np.array_equal(bq.plan(descs, V, 128, 16, order).export(), want)
     with pytest.raises(bq.BQError):
         bq.plan([(1, 256, 256, 0, 0)], 2, order=3)
+
+
+def test_adam_hparams_match_oracle(built):
+    """The library derives 1-b and the reciprocal bias corrections itself; its
+    fp32 values equal the oracle's bit for bit (so a C caller needs no arithmetic
+    of its own), and nonsense hyper-parameters come back as BQ_EINVAL."""
+    from oracle import adam8 as OA
+
+    for t in (1, 2, 10, 999, 10 ** 6):
+        for lr, b1, b2, eps in ((1e-3, 0.9, 0.999, 1e-8), (3e-4, 0.95, 0.98, 1e-6), (0.1, 0.0, 0.5, 0.0)):
+            got = bq.adam_hparams(lr, b1, b2, eps, t)
+            want = OA.adam_hparams(lr, b1, b2, eps, t)
+            for k, v in want.items():
+                assert np.float32(getattr(got, k)).tobytes() == v.tobytes(), (k, t, lr)
+    hp = bq.AdamHp()
+    for args in ((1e-3, 0.9, 0.999, 1e-8, 0), (1e-3, 1.0, 0.999, 1e-8, 1), (1e-3, 0.9, -0.1, 1e-8, 1),
+                 (float("nan"), 0.9, 0.999, 1e-8, 1), (1e-3, 0.9, 0.999, float("inf"), 1)):
+        assert built.bq_adam_hparams(*args, C.byref(hp)) == bq.BQ_EINVAL, args
+    assert built.bq_adam_hparams(1e-3, 0.9, 0.999, 1e-8, 1, None) == bq.BQ_EINVAL
