@@ -26,6 +26,7 @@ SYMBOLS = [
     "bq_layout_export", "bq_adam_hparams", "bq_layout_upload_bytes", "bq_layout_upload", "bq_shard_free", "bq_shard_check", "bq_wait_selftest", "bq_pack",
     "bq_step_adam8", "bq_quant_fp8", "bq_muon_ns_workspace", "bq_muon_ns", "bq_muon_ns_check",
     "bq_muon_ns_noalloc", "bq_muon_roots", "bq_muon_momentum", "bq_muon_apply", "bq_dequant_fp8",
+    "bq_group_place", "bq_group_upload_bytes", "bq_group_upload",
 ]
 
 
@@ -51,6 +52,18 @@ class LayoutInfo(C.Structure):
 
 class AdamHp(C.Structure):
     _fields_ = [(n, C.c_float) for n in ("lr", "b1", "b2", "eps", "omb1", "omb2", "rbc1", "rbc2")]
+
+
+class Member(C.Structure):
+    _fields_ = [("layout", C.c_void_p), ("dev_lo", C.c_int32), ("dev_hi", C.c_int32)]
+
+
+class MemberPlace(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("elem_base", "mslot_base", "fslot_base", "tensor_base")]
+
+
+class GroupInfo(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("elems", "mslots", "fslots", "tensors")]
 
 
 class Mat(C.Structure):
@@ -99,6 +112,9 @@ def load():
     lib.bq_dequant_fp8.argtypes = [P, P, P, P, P]
     lib.bq_muon_momentum.argtypes = [P, P, P, C.c_float, P, P]
     lib.bq_muon_apply.argtypes = [P, P, P, P, P]
+    lib.bq_group_place.argtypes = [C.POINTER(Member), C.c_int, C.POINTER(MemberPlace), C.POINTER(GroupInfo)]
+    lib.bq_group_upload_bytes.argtypes = [C.POINTER(Member), C.c_int, C.POINTER(C.c_size_t)]
+    lib.bq_group_upload.argtypes = [C.POINTER(Member), C.c_int, P, C.c_size_t, P, C.POINTER(P)]
     lib.bq_muon_ns_noalloc.argtypes = [C.c_int, C.POINTER(Mat), C.c_int, C.c_float, C.c_float, C.c_float,
                                        C.c_float, P]
     for name in SYMBOLS:
@@ -191,6 +207,37 @@ class Shard:
     @property
     def handle(self):
         return self._h
+
+
+class Group:
+    """Local shard ranges of several layouts stepped together (one launch per
+    kernel family).  members: list of (Layout, dev_lo, dev_hi).  ``place`` lists
+    each member's elem / mslot / fslot / tensor base in the group's buffers and
+    pointer arrays; ``info`` the group's buffer lengths."""
+
+    def __init__(self, members):
+        self.members = [(lay, int(lo), int(hi)) for lay, lo, hi in members]
+        self._arr = (Member * len(self.members))(*[Member(lay.handle.value, lo, hi) for lay, lo, hi in self.members])
+        pl = (MemberPlace * len(self.members))()
+        inf = GroupInfo()
+        _check(load().bq_group_place(self._arr, len(self.members), pl, C.byref(inf)))
+        self.place = [{n: getattr(p, n) for n, _ in MemberPlace._fields_} for p in pl]
+        self.info = {n: getattr(inf, n) for n, _ in GroupInfo._fields_}
+
+    def upload_bytes(self):
+        b = C.c_size_t()
+        _check(load().bq_group_upload_bytes(self._arr, len(self.members), C.byref(b)))
+        return b.value
+
+    def upload(self, ws, ws_bytes=None, stream=None):
+        """Device tables of the whole group into workspace ws; returns a Shard
+        that every step call accepts."""
+        if ws_bytes is None:
+            ws_bytes = ws.numel() * ws.element_size()
+        h = C.c_void_p()
+        _check(load().bq_group_upload(self._arr, len(self.members), _ptr(ws), ws_bytes, _stream(stream),
+                                      C.byref(h)))
+        return Shard(h.value, self, ws, 0, 0)
 
 
 ORDER_GIVEN, ORDER_BLOCK, ORDER_SHAPE = 0, 1, 2

@@ -110,6 +110,108 @@ int check_range(const bq_layout* L, int dev_lo, int dev_hi) {
   return BQ_OK;
 }
 
+// Stage every table in one host image, copy it with one synchronised copy (the
+// image may be freed on return) and make the host shard object pointing at it.
+int upload_tables(const ShardTables& T, void* dev_ws, size_t ws_bytes, bq_stream_t stream, const char* who,
+                  bq_shard** out) {
+  const WsPlan p = ws_plan(T);
+  if (ws_bytes < p.bytes) return set_error(BQ_ENOSPC, std::string(who) + ": workspace too small");
+  std::vector<unsigned char> img(p.bytes, 0);
+  auto put = [&](size_t off, const void* src, size_t n) {
+    if (n) std::memcpy(img.data() + off, src, n);
+  };
+  put(p.off_pieces, T.pieces.data(), T.pieces.size() * sizeof(PackPiece));
+  put(p.off_chunks, T.chunk_first.data(), T.chunk_first.size() * sizeof(int32_t));
+  put(p.off_f256, T.flat256.data(), T.flat256.size() * sizeof(FlatGroup));
+  put(p.off_f128, T.flat128.data(), T.flat128.size() * sizeof(FlatGroup));
+  put(p.off_strips, T.strips.data(), T.strips.size() * sizeof(RegionGroup));
+  put(p.off_tiles, T.tiles.data(), T.tiles.size() * sizeof(RegionGroup));
+  put(p.off_muon, T.muon.data(), T.muon.size() * sizeof(PackPiece));
+  put(p.off_f32, T.flat32.data(), T.flat32.size() * sizeof(FlatGroup));
+  put(p.off_t32, T.tiles32.data(), T.tiles32.size() * sizeof(RegionGroup));
+  put(p.off_bt, T.band_tiles.data(), T.band_tiles.size() * sizeof(RegionGroup));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(dev_ws, img.data(), p.bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string(who) + ": " + cudaGetErrorString(e));
+
+  auto* sh = new bq_shard();
+  auto* base = static_cast<unsigned char*>(dev_ws);
+  sh->dev.pieces = reinterpret_cast<const PackPiece*>(base + p.off_pieces);
+  sh->dev.chunk_first = reinterpret_cast<const int32_t*>(base + p.off_chunks);
+  sh->dev.flat256 = reinterpret_cast<const FlatGroup*>(base + p.off_f256);
+  sh->dev.flat128 = reinterpret_cast<const FlatGroup*>(base + p.off_f128);
+  sh->dev.strips = reinterpret_cast<const RegionGroup*>(base + p.off_strips);
+  sh->dev.tiles = reinterpret_cast<const RegionGroup*>(base + p.off_tiles);
+  sh->dev.muon = reinterpret_cast<const PackPiece*>(base + p.off_muon);
+  sh->dev.flat32 = reinterpret_cast<const FlatGroup*>(base + p.off_f32);
+  sh->dev.tiles32 = reinterpret_cast<const RegionGroup*>(base + p.off_t32);
+  sh->dev.band_tiles = reinterpret_cast<const RegionGroup*>(base + p.off_bt);
+  sh->dev.nchunks = T.nchunks;
+  sh->dev.n_flat256 = int32_t(T.flat256.size());
+  sh->dev.n_flat128 = int32_t(T.flat128.size());
+  sh->dev.n_strips = int32_t(T.strips.size());
+  sh->dev.n_tiles = int32_t(T.tiles.size());
+  sh->dev.n_muon = int32_t(T.muon.size());
+  sh->dev.n_flat32 = int32_t(T.flat32.size());
+  sh->dev.n_tiles32 = int32_t(T.tiles32.size());
+  sh->dev.n_band_tiles = int32_t(T.band_tiles.size());
+  sh->dev.max_strip_tiles = T.max_strip_tiles;
+  sh->dev.status = reinterpret_cast<int*>(base + p.off_status);
+  *out = sh;
+  return BQ_OK;
+}
+
+// Members' element ranges start at multiples of kGroupAlign elements (16-byte
+// aligned in every buffer, whole 256-element Adam blocks apart); slots and
+// tensors follow one another without gaps.
+constexpr int64_t kGroupAlign = 256;
+
+int group_place(const bq_member* members, int n, std::vector<bq_member_place>& pl, bq_group_info& gi) {
+  if (!members || n < 1) return set_error(BQ_EINVAL, "bq_group: need at least one member");
+  pl.assign(size_t(n), bq_member_place{0, 0, 0, 0});
+  int64_t elem = 0, ms = 0, fs = 0, nt = 0, end = 0;
+  for (int u = 0; u < n; ++u) {
+    const bq_layout* L = members[u].layout;
+    const int lo = members[u].dev_lo, hi = members[u].dev_hi;
+    if (int rc = check_range(L, lo, hi)) return rc;
+    elem = align_up(size_t(end), size_t(kGroupAlign));
+    pl[u] = bq_member_place{elem, ms, fs, nt};
+    end = elem + int64_t(hi - lo) * L->S;
+    ms += L->dev_mslot[hi] - L->dev_mslot[lo];
+    fs += L->dev_fslot[hi] - L->dev_fslot[lo];
+    nt += int64_t(L->tensors.size());
+  }
+  if (end > (int64_t(1) << 40) || ms >= (int64_t(1) << 31) || fs >= (int64_t(1) << 31) || nt >= (int64_t(1) << 31))
+    return set_error(BQ_EINVAL, "bq_group: group too large (2^40 elements, 2^31 slots or tensors)");
+  gi = bq_group_info{end, ms, fs, nt};
+  return BQ_OK;
+}
+
+int build_group(const bq_member* members, int n, ShardTables& G, bq_group_info& gi) {
+  std::vector<bq_member_place> pl;
+  if (int rc = group_place(members, n, pl, gi)) return rc;
+  for (int u = 0; u < n; ++u) {
+    const bq_layout& L = *members[u].layout;
+    ShardTables M;
+    build_shard_tables(L, members[u].dev_lo, members[u].dev_hi, M);
+    const std::string bad = validate_shard_tables(L, members[u].dev_lo, members[u].dev_hi, M);
+    if (!bad.empty())
+      return set_error(BQ_EINVAL, "bq_group: internal table check of member " + std::to_string(u) + " failed: " + bad);
+    append_member_tables(M, GroupPlace{pl[u].elem_base, pl[u].mslot_base, pl[u].fslot_base, pl[u].tensor_base}, G);
+  }
+  finish_group_tables(gi.elems, G);
+  // the concatenation itself: pieces tile [0, elems) inside their chunks
+  int64_t cursor = 0;
+  for (const PackPiece& q : G.pieces) {
+    if (q.dst != cursor || q.len <= 0 || q.dst / kPackChunk != (q.dst + q.len - 1) / kPackChunk)
+      return set_error(BQ_EINVAL, "bq_group: internal check failed: pack pieces do not tile the group");
+    cursor += q.len;
+  }
+  if (cursor != gi.elems) return set_error(BQ_EINVAL, "bq_group: internal check failed: pack pieces do not cover the group");
+  return BQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -152,59 +254,51 @@ int bq_layout_upload(const bq_layout* L, int dev_lo, int dev_hi, void* dev_ws, s
   build_shard_tables(*L, dev_lo, dev_hi, T);
   const std::string bad = validate_shard_tables(*L, dev_lo, dev_hi, T);
   if (!bad.empty()) return set_error(BQ_EINVAL, "bq_layout_upload: internal table check failed: " + bad);
-  const WsPlan p = ws_plan(T);
-  if (ws_bytes < p.bytes) return set_error(BQ_ENOSPC, "bq_layout_upload: workspace too small");
-  // stage everything in one host image, one copy, synchronised so the host image
-  // may be freed on return
-  std::vector<unsigned char> img(p.bytes, 0);
-  auto put = [&](size_t off, const void* src, size_t n) {
-    if (n) std::memcpy(img.data() + off, src, n);
-  };
-  put(p.off_pieces, T.pieces.data(), T.pieces.size() * sizeof(PackPiece));
-  put(p.off_chunks, T.chunk_first.data(), T.chunk_first.size() * sizeof(int32_t));
-  put(p.off_f256, T.flat256.data(), T.flat256.size() * sizeof(FlatGroup));
-  put(p.off_f128, T.flat128.data(), T.flat128.size() * sizeof(FlatGroup));
-  put(p.off_strips, T.strips.data(), T.strips.size() * sizeof(RegionGroup));
-  put(p.off_tiles, T.tiles.data(), T.tiles.size() * sizeof(RegionGroup));
-  put(p.off_muon, T.muon.data(), T.muon.size() * sizeof(PackPiece));
-  put(p.off_f32, T.flat32.data(), T.flat32.size() * sizeof(FlatGroup));
-  put(p.off_t32, T.tiles32.data(), T.tiles32.size() * sizeof(RegionGroup));
-  put(p.off_bt, T.band_tiles.data(), T.band_tiles.size() * sizeof(RegionGroup));
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(dev_ws, img.data(), p.bytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return set_error(BQ_ECUDA, std::string("bq_layout_upload: ") + cudaGetErrorString(e));
+  const int64_t total = int64_t(dev_hi - dev_lo) * L->S;
+  const int64_t nm = L->dev_mslot[dev_hi] - L->dev_mslot[dev_lo];
+  const int64_t nf = L->dev_fslot[dev_hi] - L->dev_fslot[dev_lo];
+  if (int rc = upload_tables(T, dev_ws, ws_bytes, stream, "bq_layout_upload", out)) return rc;
+  (*out)->layout = L;
+  (*out)->dev_lo = dev_lo;
+  (*out)->dev_hi = dev_hi;
+  (*out)->total = total;
+  (*out)->nm = nm;
+  (*out)->nf = nf;
+  return BQ_OK;
+}
 
-  auto* sh = new bq_shard();
-  sh->layout = L;
-  sh->dev_lo = dev_lo;
-  sh->dev_hi = dev_hi;
-  sh->total = int64_t(dev_hi - dev_lo) * L->S;
-  sh->nm = L->dev_mslot[dev_hi] - L->dev_mslot[dev_lo];
-  sh->nf = L->dev_fslot[dev_hi] - L->dev_fslot[dev_lo];
-  auto* base = static_cast<unsigned char*>(dev_ws);
-  sh->dev.pieces = reinterpret_cast<const PackPiece*>(base + p.off_pieces);
-  sh->dev.chunk_first = reinterpret_cast<const int32_t*>(base + p.off_chunks);
-  sh->dev.flat256 = reinterpret_cast<const FlatGroup*>(base + p.off_f256);
-  sh->dev.flat128 = reinterpret_cast<const FlatGroup*>(base + p.off_f128);
-  sh->dev.strips = reinterpret_cast<const RegionGroup*>(base + p.off_strips);
-  sh->dev.tiles = reinterpret_cast<const RegionGroup*>(base + p.off_tiles);
-  sh->dev.muon = reinterpret_cast<const PackPiece*>(base + p.off_muon);
-  sh->dev.flat32 = reinterpret_cast<const FlatGroup*>(base + p.off_f32);
-  sh->dev.tiles32 = reinterpret_cast<const RegionGroup*>(base + p.off_t32);
-  sh->dev.band_tiles = reinterpret_cast<const RegionGroup*>(base + p.off_bt);
-  sh->dev.nchunks = T.nchunks;
-  sh->dev.n_flat256 = int32_t(T.flat256.size());
-  sh->dev.n_flat128 = int32_t(T.flat128.size());
-  sh->dev.n_strips = int32_t(T.strips.size());
-  sh->dev.n_tiles = int32_t(T.tiles.size());
-  sh->dev.n_muon = int32_t(T.muon.size());
-  sh->dev.n_flat32 = int32_t(T.flat32.size());
-  sh->dev.n_tiles32 = int32_t(T.tiles32.size());
-  sh->dev.n_band_tiles = int32_t(T.band_tiles.size());
-  sh->dev.max_strip_tiles = T.max_strip_tiles;
-  sh->dev.status = reinterpret_cast<int*>(base + p.off_status);
-  *out = sh;
+int bq_group_place(const bq_member* members, int n, bq_member_place* place, bq_group_info* info) {
+  std::vector<bq_member_place> pl;
+  bq_group_info gi;
+  if (int rc = group_place(members, n, pl, gi)) return rc;
+  if (place)
+    for (int u = 0; u < n; ++u) place[u] = pl[u];
+  if (info) *info = gi;
+  return BQ_OK;
+}
+
+int bq_group_upload_bytes(const bq_member* members, int n, size_t* bytes) {
+  if (!bytes) return set_error(BQ_EINVAL, "bq_group_upload_bytes: bytes is NULL");
+  ShardTables G;
+  bq_group_info gi;
+  if (int rc = build_group(members, n, G, gi)) return rc;
+  *bytes = ws_plan(G).bytes;
+  return BQ_OK;
+}
+
+int bq_group_upload(const bq_member* members, int n, void* dev_ws, size_t ws_bytes, bq_stream_t stream,
+                    bq_shard** out) {
+  if (!out) return set_error(BQ_EINVAL, "bq_group_upload: out is NULL");
+  *out = nullptr;
+  if (!dev_ws || !aligned16(dev_ws)) return set_error(BQ_EALIGN, "bq_group_upload: workspace NULL or misaligned");
+  ShardTables G;
+  bq_group_info gi;
+  if (int rc = build_group(members, n, G, gi)) return rc;
+  if (int rc = upload_tables(G, dev_ws, ws_bytes, stream, "bq_group_upload", out)) return rc;
+  (*out)->layout = nullptr;
+  (*out)->total = gi.elems;
+  (*out)->nm = gi.mslots;
+  (*out)->nf = gi.fslots;
   return BQ_OK;
 }
 

@@ -109,6 +109,13 @@ struct ShardTables {
 void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables& T);
 std::string validate_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, const ShardTables& T);
 
+// where one member of a group lives in the group's buffers and pointer arrays
+struct GroupPlace {
+  int64_t elem, mslot, fslot, tensor;
+};
+void append_member_tables(const ShardTables& member, const GroupPlace& at, ShardTables& group);
+void finish_group_tables(int64_t group_total, ShardTables& group);
+
 // ---------------------------------------------------------------- kernel launchers (step_kernels.cu)
 
 struct DevTables {

@@ -539,4 +539,74 @@ std::string validate_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, co
   return std::string();
 }
 
+// ---------------------------------------------------------------- groups of shard ranges
+// A group is several (layout, [dev_lo, dev_hi)) members stepped by one launch
+// per kernel family: every member's tables are built and checked alone, then
+// appended with its element, slot and tensor bases added.  Pack pieces are cut
+// again at the group's chunk edges, and the alignment gaps between members
+// become padding pieces (zeroed by the pack like any padding).
+
+void append_member_tables(const ShardTables& M, const GroupPlace& at, ShardTables& G) {
+  auto emit = [&](int64_t dst, int64_t len, int32_t tensor, int64_t src) {
+    while (len > 0) {
+      const int64_t chunk_end = (dst / kPackChunk + 1) * kPackChunk;
+      const int64_t n = std::min(len, chunk_end - dst);
+      G.pieces.push_back(PackPiece{dst, src, int32_t(n), tensor});
+      dst += n;
+      src += n;
+      len -= n;
+    }
+  };
+  const int64_t cursor = G.pieces.empty() ? 0 : G.pieces.back().dst + G.pieces.back().len;
+  if (at.elem > cursor) emit(cursor, at.elem - cursor, -1, 0);  // gap before the member
+  for (const PackPiece& q : M.pieces)
+    emit(at.elem + q.dst, q.len, q.tensor < 0 ? -1 : int32_t(q.tensor + at.tensor), q.src);
+  auto flat = [&](const std::vector<FlatGroup>& src, std::vector<FlatGroup>& dst) {
+    for (FlatGroup g : src) {
+      g.pos += at.elem;
+      g.mslot += int32_t(at.mslot);
+      if (g.fslot >= 0) g.fslot += int32_t(at.fslot);
+      dst.push_back(g);
+    }
+  };
+  auto region = [&](const std::vector<RegionGroup>& src, std::vector<RegionGroup>& dst, bool mslots) {
+    for (RegionGroup g : src) {
+      g.pos += at.elem;
+      if (mslots) g.mslot += int32_t(at.mslot);
+      if (g.fslot >= 0) g.fslot += int32_t(at.fslot);
+      dst.push_back(g);
+    }
+  };
+  flat(M.flat256, G.flat256);
+  flat(M.flat128, G.flat128);
+  flat(M.flat32, G.flat32);
+  region(M.strips, G.strips, true);
+  region(M.tiles, G.tiles, true);
+  region(M.tiles32, G.tiles32, true);
+  region(M.band_tiles, G.band_tiles, false);  // band FP8 tiles carry no Adam slot
+  for (PackPiece q : M.muon) {
+    q.dst += at.elem;
+    q.tensor += int32_t(at.tensor);
+    G.muon.push_back(q);
+  }
+  G.max_strip_tiles = std::max(G.max_strip_tiles, M.max_strip_tiles);
+}
+
+void finish_group_tables(int64_t group_total, ShardTables& G) {
+  const int64_t cursor = G.pieces.empty() ? 0 : G.pieces.back().dst + G.pieces.back().len;
+  for (int64_t dst = cursor; dst < group_total;) {  // trailing gap: padding
+    const int64_t n = std::min(group_total - dst, (dst / kPackChunk + 1) * kPackChunk - dst);
+    G.pieces.push_back(PackPiece{dst, 0, int32_t(n), -1});
+    dst += n;
+  }
+  G.nchunks = ceil_div(group_total, kPackChunk);
+  G.chunk_first.assign(size_t(G.nchunks) + 1, 0);
+  size_t p = 0;
+  for (int64_t c = 0; c < G.nchunks; ++c) {
+    while (p < G.pieces.size() && G.pieces[p].dst < c * kPackChunk) ++p;
+    G.chunk_first[c] = int32_t(p);
+  }
+  G.chunk_first[G.nchunks] = int32_t(G.pieces.size());
+}
+
 }  // namespace bq

@@ -151,6 +151,51 @@ int bq_layout_upload(const bq_layout* layout, int dev_lo, int dev_hi, void* dev_
                      bq_stream_t stream, bq_shard** out);
 void bq_shard_free(bq_shard* shard);
 
+/* ------------------------------------------------------------------ groups of shard ranges
+ * A group steps the local shards of several layouts at once - e.g. every
+ * fully_shard unit of a model's slice on one rank - with one launch per kernel
+ * family instead of one per unit.  Defined by: DBuffer's group-level fused
+ * operations (feynmanwiki walkthrough, paper section 5, DBuffer paragraphs:
+ * one fused launch over the whole buffer instead of per-tensor launches),
+ * carried from one DBuffer to a list of them.
+ * Member u = local shards [dev_lo, dev_hi) of `layout`.  Its place in the
+ * group's buffers (bq_group_place):
+ *   element buffers (gradient DBuffer, master, m, v, FP8 staging): the member's
+ *     element x (as in a single upload of that range) lives at elem_base + x;
+ *     elem_base is a multiple of 256 and the gaps between members are padding
+ *     (zeroed by bq_pack, untouched by the other calls);
+ *   Adam / FP8 scale buffers: the member's slot z at mslot_base / fslot_base + z;
+ *   per-tensor pointer and lr arrays (bq_pack, bq_muon_*): the member's tensor i
+ *     at entry tensor_base + i.
+ * info->elems, mslots, fslots, tensors: the group's buffer lengths.
+ * bq_group_upload builds and checks every member's tables, concatenates them
+ * with those offsets into the caller's device workspace (ws_bytes from
+ * bq_group_upload_bytes; one synchronised copy) and returns a bq_shard that
+ * bq_pack, bq_step_adam8, bq_quant_fp8, bq_dequant_fp8, bq_muon_momentum,
+ * bq_muon_apply and bq_shard_check accept like any other (its "range" is the
+ * whole group).  The layouts may be freed after the upload (the tables are
+ * copied).  The same layout may appear in several members (identical units).
+ * Errors: BQ_EINVAL (n < 1, a NULL layout, a bad range, or a group above 2^40
+ * elements / 2^31 slots or tensors), BQ_EALIGN (as bq_layout_upload),
+ * BQ_ENOSPC (workspace too small), BQ_ECUDA. */
+typedef struct {
+  const bq_layout* layout;
+  int32_t dev_lo, dev_hi;
+} bq_member;
+
+typedef struct {
+  int64_t elem_base, mslot_base, fslot_base, tensor_base;
+} bq_member_place;
+
+typedef struct {
+  int64_t elems, mslots, fslots, tensors;
+} bq_group_info;
+
+int bq_group_place(const bq_member* members, int n, bq_member_place* place, bq_group_info* info);
+int bq_group_upload_bytes(const bq_member* members, int n, size_t* bytes);
+int bq_group_upload(const bq_member* members, int n, void* dev_ws, size_t ws_bytes, bq_stream_t stream,
+                    bq_shard** out);
+
 /* bq_shard_check - synchronise `stream` and read the shard's device error word
  * (kept in its workspace): the 2-D Adam kernel's producer / consumer waits give
  * up after about a second, record where (1, 2: the copy producer; 3: a compute

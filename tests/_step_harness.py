@@ -211,3 +211,181 @@ def sampled_check(case, got, n_blocks=300, n_tiles=24, seed=0):
         assert_bits_equal(f"fp8 codes tile {tslot} (standalone)", got["q2"][tpos], q)
         done += 1
     assert done > 0
+
+
+GAP_BF16, GAP_F32, GAP_I8, GAP_U8 = 0x3F80, np.float32(-777.0), np.int8(-55), np.uint8(200)
+
+
+def run_group_gpu(cases, dev, scale, fp8=True, graph=False):
+    """The DBuffer step of several StepCases as ONE group (bq.Group): their
+    inputs placed at the group's bases in shared buffers (sentinels in the gaps
+    between members), one pack, one Adam (+ FP8) and one standalone FP8 call over
+    the whole group, optionally captured in a CUDA graph and replayed.  Returns
+    per-case outputs (the same keys as StepCase.run_gpu) and the gap contents."""
+    grp = bq.Group([(c.layout, c.dev_lo, c.dev_hi) for c in cases])
+    E, M, F, NT = (grp.info[k] for k in ("elems", "mslots", "fslots", "tensors"))
+    dbuf0 = np.full(E, GAP_BF16, np.uint16)
+    master = np.full(E, GAP_F32, np.float32)
+    m = np.full(E, GAP_I8, np.int8)
+    v = np.full(E, GAP_U8, np.uint8)
+    fp8_0 = np.full(E, 0xAA, np.uint8)
+    ms, vs = np.zeros(max(M, 1), np.float32), np.zeros(max(M, 1), np.float32)
+    fs0 = np.full(max(F, 1), np.nan, np.float32)
+    ptrs = np.zeros(max(NT, 1), np.int64)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    gbufs = []
+    for c, p in zip(cases, grp.place):
+        e0, m0, f0, t0 = p["elem_base"], p["mslot_base"], p["fslot_base"], p["tensor_base"]
+        dbuf0[e0:e0 + c.n] = c.dbuf0
+        master[e0:e0 + c.n] = c.master
+        m[e0:e0 + c.n] = c.m
+        v[e0:e0 + c.n] = c.v
+        fp8_0[e0:e0 + c.n] = c.fp8_0
+        ms[m0:m0 + c.nm] = c.ms
+        vs[m0:m0 + c.nm] = c.vs
+        fs0[f0:f0 + c.nf] = c.fs0[:c.nf]
+        for i, (bits, lo) in c.grads.items():
+            g = d(bits.view(np.int16))
+            gbufs.append(g)
+            ptrs[t0 + i] = g.data_ptr() - 2 * lo
+    hps = {(c.cfg.lr, c.cfg.b1, c.cfg.b2, c.cfg.eps, c.t) for c in cases}
+    assert len(hps) == 1, "one group step takes one set of hyper-parameters"
+    s = torch.cuda.Stream(dev)
+    ws = torch.empty(grp.upload_bytes(), dtype=torch.uint8, device=dev)
+    shard = grp.upload(ws, stream=s)
+    gp = d(ptrs)
+    t_dbuf, t_master, t_m, t_v = d(dbuf0.view(np.int16)), d(master), d(m), d(v)
+    t_ms, t_vs = d(ms), d(vs)
+    t_fp8 = d(fp8_0) if fp8 else None
+    t_fs = d(fs0) if fp8 else None
+    q2, s2 = d(fp8_0), d(fs0)
+    hp = cases[0].hp_c
+    sc = float(scale)  # one pack scale for the whole group
+
+    def step(stream):
+        bq.pack(shard, gp, t_dbuf, sc, False, stream=stream)
+        bq.step_adam8(shard, t_dbuf, t_master, t_m, t_v, t_ms, t_vs, hp, t_fp8, t_fs, stream=stream)
+        bq.quant_fp8(shard, t_master, q2, s2, stream=stream)
+
+    torch.cuda.synchronize(dev)
+    if graph:
+        # an eager step first (first launches set kernel attributes, which stay
+        # out of the capture), then every buffer back to its initial contents
+        step(s)
+        torch.cuda.synchronize(dev)
+        for t, a in ((t_dbuf, dbuf0.view(np.int16)), (t_master, master), (t_m, m), (t_v, v), (t_ms, ms), (t_vs, vs),
+                     (t_fp8, fp8_0), (t_fs, fs0), (q2, fp8_0), (s2, fs0)):
+            if t is not None:
+                t.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(s):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                step(s)
+            g.replay()
+    else:
+        step(s)
+    bq.shard_check(shard, stream=s)
+    torch.cuda.synchronize(dev)
+    h = lambda t: None if t is None else t.cpu().numpy()  # noqa: E731
+    full = dict(dbuf=h(t_dbuf).view(np.uint16), master=h(t_master), m=h(t_m), v=h(t_v), ms=h(t_ms), vs=h(t_vs),
+                fp8=h(t_fp8), fs=h(t_fs), q2=h(q2), s2=h(s2))
+    outs = []
+    inside = np.zeros(E, bool)
+    for c, p in zip(cases, grp.place):
+        e0, m0, f0 = p["elem_base"], p["mslot_base"], p["fslot_base"]
+        inside[e0:e0 + c.n] = True
+        o = {}
+        for k in ("dbuf", "master", "m", "v", "fp8", "q2"):
+            o[k] = None if full[k] is None else full[k][e0:e0 + c.n]
+        o["ms"], o["vs"] = full["ms"][m0:m0 + c.nm], full["vs"][m0:m0 + c.nm]
+        for k in ("fs", "s2"):  # the member's FP8 slots only (there may be none)
+            o[k] = None if full[k] is None else full[k][f0:f0 + c.nf]
+        outs.append(o)
+    gaps = {k: full[k][~inside] for k in ("dbuf", "master", "m", "v", "q2")}
+    if fp8:
+        gaps["fp8"] = full["fp8"][~inside]
+    del gbufs
+    return outs, gaps, grp
+
+
+def run_model_group_gpu(cfg, dev, sample_members):
+    """Every unit of a model's rank-range slice as ONE group, as the benchmark
+    steps it: one StepCase per distinct unit (identical units, e.g. the layers,
+    share that case's inputs), the inputs placed at each member's base in
+    device buffers of the group's size, one pack + Adam (+ FP8) + standalone FP8
+    call over the group.  Returns (cases, member -> case index, outputs of the
+    members in sample_members as StepCase.run_gpu returns them, a function
+    that tells whether two members' outputs are identical on the device)."""
+    cases = [StepCase(cfg, unit_index=u) for u in range(len(cfg.units))]
+    member_case = [u for u, unit in enumerate(cfg.units) for _ in range(unit.repeat)]
+    grp = bq.Group([(cases[u].layout, cases[u].dev_lo, cases[u].dev_hi) for u in member_case])
+    E, M, F, NT = (grp.info[k] for k in ("elems", "mslots", "fslots", "tensors"))
+    s = torch.cuda.Stream(dev)
+    dbuf = torch.full((E,), GAP_BF16, dtype=torch.int16, device=dev)
+    master = torch.full((E,), float(GAP_F32), dtype=torch.float32, device=dev)
+    m = torch.full((E,), int(GAP_I8), dtype=torch.int8, device=dev)
+    v = torch.full((E,), int(GAP_U8), dtype=torch.uint8, device=dev)
+    fp8 = torch.full((E,), 0xAA, dtype=torch.uint8, device=dev)
+    q2 = torch.full((E,), 0xAA, dtype=torch.uint8, device=dev)
+    ms = torch.zeros(max(M, 1), dtype=torch.float32, device=dev)
+    vs = torch.zeros(max(M, 1), dtype=torch.float32, device=dev)
+    fs = torch.full((max(F, 1),), float("nan"), dtype=torch.float32, device=dev)
+    s2 = torch.full((max(F, 1),), float("nan"), dtype=torch.float32, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))  # noqa: E731
+    gdev = {}  # distinct case -> device gradients (read only, shared by identical members)
+    ptrs = np.zeros(max(NT, 1), np.int64)
+    for u, p in zip(member_case, grp.place):
+        c = cases[u]
+        e0, m0, f0, t0 = p["elem_base"], p["mslot_base"], p["fslot_base"], p["tensor_base"]
+        if u not in gdev:
+            gdev[u] = {i: (t(bits.view(np.int16)).to(dev), lo) for i, (bits, lo) in c.grads.items()}
+        for i, (g, lo) in gdev[u].items():
+            ptrs[t0 + i] = g.data_ptr() - 2 * lo
+        dbuf[e0:e0 + c.n].copy_(t(c.dbuf0.view(np.int16)))
+        master[e0:e0 + c.n].copy_(t(c.master))
+        m[e0:e0 + c.n].copy_(t(c.m))
+        v[e0:e0 + c.n].copy_(t(c.v))
+        ms[m0:m0 + c.nm].copy_(t(c.ms))
+        vs[m0:m0 + c.nm].copy_(t(c.vs))
+    gp = t(ptrs).to(dev)
+    ws = torch.empty(grp.upload_bytes(), dtype=torch.uint8, device=dev)
+    shard = grp.upload(ws, stream=s)
+    torch.cuda.synchronize(dev)
+    bq.pack(shard, gp, dbuf, 1.0 / cfg.V, False, stream=s)
+    bq.step_adam8(shard, dbuf, master, m, v, ms, vs, cases[0].hp_c, fp8, fs, stream=s)
+    bq.quant_fp8(shard, master, q2, s2, stream=s)
+    bq.shard_check(shard, stream=s)
+    torch.cuda.synchronize(dev)
+
+    def member_out(j):
+        c, p = cases[member_case[j]], grp.place[j]
+        e0, m0, f0 = p["elem_base"], p["mslot_base"], p["fslot_base"]
+        h = lambda x, a, n: x[a:a + n].cpu().numpy()  # noqa: E731
+        return dict(dbuf=h(dbuf, e0, c.n).view(np.uint16), master=h(master, e0, c.n), m=h(m, e0, c.n),
+                    v=h(v, e0, c.n), ms=h(ms, m0, c.nm), vs=h(vs, m0, c.nm), fp8=h(fp8, e0, c.n),
+                    fs=h(fs, f0, max(c.nf, 1)), q2=h(q2, e0, c.n), s2=h(s2, f0, max(c.nf, 1)))
+
+    def same(j, k):
+        pj, pk = grp.place[j], grp.place[k]
+        c = cases[member_case[j]]
+        assert member_case[j] == member_case[k]
+        for x in (dbuf, master, m, v, fp8, q2):
+            if not torch.equal(x[pj["elem_base"]:pj["elem_base"] + c.n], x[pk["elem_base"]:pk["elem_base"] + c.n]):
+                return False
+        for x, b in ((ms, "mslot_base"), (vs, "mslot_base"), (fs, "fslot_base"), (s2, "fslot_base")):
+            n = c.nm if b == "mslot_base" else c.nf
+            if not torch.equal(x[pj[b]:pj[b] + n], x[pk[b]:pk[b] + n]):
+                return False
+        return True
+
+    # gaps between members: zeroed in the gradient DBuffer, untouched elsewhere
+    inside = torch.zeros(E, dtype=torch.bool, device=dev)
+    for u, p in zip(member_case, grp.place):
+        inside[p["elem_base"]:p["elem_base"] + cases[u].n] = True
+    gaps = ~inside
+    assert not torch.any(dbuf[gaps] != 0)
+    assert torch.all(master[gaps] == float(GAP_F32)) and torch.all(m[gaps] == int(GAP_I8))
+    assert torch.all(fp8[gaps] == 0xAA) and torch.all(q2[gaps] == 0xAA)
+    outs = {j: member_out(j) for j in sample_members}
+    return cases, member_case, outs, same

@@ -252,3 +252,35 @@ def test_adam_hparams_match_oracle(built):
                  (float("nan"), 0.9, 0.999, 1e-8, 1), (1e-3, 0.9, 0.999, float("inf"), 1)):
         assert built.bq_adam_hparams(*args, C.byref(hp)) == bq.BQ_EINVAL, args
     assert built.bq_adam_hparams(1e-3, 0.9, 0.999, 1e-8, 1, None) == bq.BQ_EINVAL
+
+
+def test_group_place_and_errors(built):
+    """Member bases in a group: elements at multiples of 256 in member order
+    (each after the previous member's range), slots and tensors back to back;
+    a NULL layout, an empty group or a bad range is refused."""
+    c = W.config("llama-small")
+    lay = bq.plan(c.units[0].tensors, c.V, c.alpha, c.start_align)
+    toy = W.config("toy")
+    lay2 = bq.plan(toy.units[0].tensors, toy.V, toy.alpha, toy.start_align)
+    T, T2 = W.Table(lay.export()), W.Table(lay2.export())
+    members = [(lay, 0, 8), (lay2, 1, 3), (lay, 3, 5)]
+    g = bq.Group(members)
+    end = ms = fs = nt = 0
+    for (L, lo, hi), tab, p in zip(members, (T, T2, T), g.place):
+        eb = -(-end // 256) * 256
+        assert p == dict(elem_base=eb, mslot_base=ms, fslot_base=fs, tensor_base=nt)
+        end = eb + (hi - lo) * tab.S
+        a, b = tab.slot_range(lo, hi)
+        ms += b - a
+        a, b = tab.slot_range(lo, hi, fp8=True)
+        fs += b - a
+        nt += tab.N
+    assert g.info == dict(elems=end, mslots=ms, fslots=fs, tensors=nt)
+    assert g.upload_bytes() > 0
+    bad = (bq.Member * 1)(bq.Member(None, 0, 1))
+    assert built.bq_group_place(bad, 1, None, None) == bq.BQ_EINVAL
+    assert built.bq_group_place(bad, 0, None, None) == bq.BQ_EINVAL
+    bad = (bq.Member * 1)(bq.Member(lay.handle.value, 5, 9))
+    assert built.bq_group_place(bad, 1, None, None) == bq.BQ_EINVAL
+    n = C.c_size_t()
+    assert built.bq_group_upload_bytes(bad, 1, C.byref(n)) == bq.BQ_EINVAL

@@ -1,7 +1,8 @@
 """The DBuffer step of several units captured in one CUDA graph: replaying the
-graph gives bit for bit what the same calls give launched one by one (and the
-eager result is the oracle's, checked elsewhere).  Covers the TMA-fed strip
-kernel, the 128x128 and 32x32 tile kernels and the flat kernels inside a graph."""
+graph gives bit for bit the oracle's result (and what the same calls give
+launched one by one); a second replay equals the oracle's second step.  Covers
+the TMA-fed strip kernel, the 128x128 and 32x32 tile kernels and the flat
+kernels inside a graph, serial and on branches."""
 
 import numpy as np
 import pytest
@@ -39,7 +40,29 @@ class DeviceUnit:
                       self.fp8, self.fs, stream=stream)
 
     def outputs(self):
-        return {k: getattr(self, k).cpu().numpy() for k in ("dbuf", "master", "m", "v", "ms", "vs", "fp8", "fs")}
+        out = {k: getattr(self, k).cpu().numpy() for k in ("dbuf", "master", "m", "v", "ms", "vs", "fp8", "fs")}
+        out["dbuf"] = out["dbuf"].view(np.uint16)
+        return out
+
+
+def _oracle_two_steps(case):
+    """The oracle's first step, and its second step from the first one's state
+    (same gradients, same hyper-parameters, as a replay does)."""
+    from oracle import adam8 as OA
+    from oracle import fp8 as OF
+
+    one = case.run_oracle()
+    L, lo, hi = case.olayout, case.dev_lo, case.dev_hi
+    master, m, v, ms, vs = OA.adam8_step(L, lo, hi, one["dbuf"], one["master"], one["m"], one["v"], one["ms"],
+                                         one["vs"], case.hp_o)
+    q, fs = OF.quant_fp8(L, lo, hi, master, one["fp8"], one["fs"])
+    two = dict(dbuf=one["dbuf"], master=master, m=m, v=v, ms=ms, vs=vs, fp8=q, fs=fs)
+    return one, two
+
+
+def _check_against(name, got, want):
+    for k in ("dbuf", "master", "m", "v", "ms", "vs", "fp8", "fs"):
+        assert_bits_equal(f"{name} {k}", got[k], want[k])
 
 
 def test_model_step_graph_replay_matches_eager(cuda):
@@ -58,20 +81,23 @@ def test_model_step_graph_replay_matches_eager(cuda):
             u.step(stream)
     g.replay()
     torch.cuda.synchronize(cuda)
-    for c, a, b in zip(cases, eager, graphed):
+    oracle = [_oracle_two_steps(c) for c in cases]
+    for c, a, b, (one, _) in zip(cases, eager, graphed, oracle):
         bq.shard_check(a.shard)
         bq.shard_check(b.shard)
         oa, ob = a.outputs(), b.outputs()
+        _check_against(f"{c.cfg.name} graph vs oracle", ob, one)
         for k in oa:
             assert_bits_equal(f"{c.cfg.name} {k}", ob[k], oa[k])
-    # a second replay continues from the updated state exactly like a second eager step
+    # a second replay continues from the updated state: the oracle's second step
     with torch.cuda.stream(stream):
         for u in eager:
             u.step(stream)
     g.replay()
     torch.cuda.synchronize(cuda)
-    for c, a, b in zip(cases, eager, graphed):
+    for c, a, b, (_, two) in zip(cases, eager, graphed, oracle):
         oa, ob = a.outputs(), b.outputs()
+        _check_against(f"{c.cfg.name} graph step 2 vs oracle", ob, two)
         for k in ("master", "m", "v", "ms", "vs", "fp8", "fs"):
             assert_bits_equal(f"{c.cfg.name} {k} (step 2)", ob[k], oa[k])
 
@@ -107,5 +133,6 @@ def test_branched_graph_matches_eager(cuda):
     for c, a, b in zip(cases, eager, graphed):
         bq.shard_check(b.shard)
         oa, ob = a.outputs(), b.outputs()
+        _check_against(f"{c.cfg.name} branched graph vs oracle", ob, c.run_oracle())
         for k in oa:
             assert_bits_equal(f"{c.cfg.name} {k} (branched)", ob[k], oa[k])
