@@ -19,8 +19,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "bq_internal.h"
 #include "tmem_ptx.h"
@@ -601,21 +603,111 @@ int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs
   return check("bq_muon_ns (gemm)");
 }
 
-}  // namespace
-
-int muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes) {
-  if (!bytes || batch < 0 || (batch > 0 && !mats)) return set_error(BQ_EINVAL, "bq_muon_ns_workspace: bad arguments");
-  size_t need = 256;
+// Matrix i's workspace region in the concurrent layout starts at region_off[i]
+// (1024-byte multiples; region 0 at 0 holds the batch's error word).
+size_t concurrent_bytes(int batch, const bq_mat* mats, std::vector<size_t>* region_off) {
+  size_t o = 0;
   for (int i = 0; i < batch; ++i) {
-    if (int rc = check_mat(mats[i])) return rc;
-    need = std::max(need, ns_plan(mats[i]).bytes);
+    if (region_off) region_off->push_back(o);
+    o += (ns_plan(mats[i]).bytes + 1023) / 1024 * 1024;
   }
-  *bytes = need;
-  return BQ_OK;
+  return std::max<size_t>(o, 256);
 }
 
-int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws, size_t ws_bytes,
-            void* stream) {
+// One matrix's whole Newton-Schulz on stream s: workspace region w (its own
+// scratch), error word `status` (the batch's).
+int ns_one(const bq_mat& t, unsigned char* w, int* status, int steps, float a, float b, float c, float eps,
+           cudaStream_t s) {
+  const NsPlan p = ns_plan(t);
+  float* part = reinterpret_cast<float*>(w + p.off_part);
+  float* inv = reinterpret_cast<float*>(w + p.off_status + 16);  // 1 / (||x||_F + eps)
+  auto* X0 = reinterpret_cast<__nv_bfloat16*>(w + p.off_x0);
+  auto* X1 = reinterpret_cast<__nv_bfloat16*>(w + p.off_x1);
+  auto* A = reinterpret_cast<__nv_bfloat16*>(w + p.off_a);
+  auto* B = reinterpret_cast<__nv_bfloat16*>(w + p.off_b);
+  const auto* x = static_cast<const __nv_bfloat16*>(t.x);
+  auto* y = static_cast<__nv_bfloat16*>(t.y);
+
+  // normalise into X0 (transposed for a tall input)
+  k_sumsq<<<kRedBlocks, kRedThreads, 0, s>>>(x, t.rows, t.cols, t.ld_x, part);
+  if (int rc = check("bq_muon_ns (norm)")) return rc;
+  const dim3 cg(unsigned((t.cols + kCopyTile - 1) / kCopyTile), unsigned((t.rows + kCopyTile - 1) / kCopyTile));
+  k_inv_norm<<<1, kRedThreads, 0, s>>>(part, kRedBlocks, eps, inv);
+  if (int rc = check("bq_muon_ns (inv norm)")) return rc;
+  k_scale_copy<<<cg, 256, 0, s>>>(x, t.rows, t.cols, t.ld_x, X0, p.ldx, p.tall ? 1 : 0, inv);
+  if (int rc = check("bq_muon_ns (scale)")) return rc;
+
+  // tensor maps: X as K-major A operand / K-major B operand / MN-major B operand, A, B
+  CUtensorMap mXa[2], mXb[2], mXmn[2], mAa, mAb, mBa;
+  __nv_bfloat16* Xs[2] = {X0, X1};
+  for (int j = 0; j < 2; ++j) {
+    if (int rc = make_map(&mXa[j], Xs[j], p.n, p.m, p.ldx, BM)) return rc;
+    if (int rc = make_map(&mXb[j], Xs[j], p.n, p.m, p.ldx, BN)) return rc;
+    if (int rc = make_map(&mXmn[j], Xs[j], p.n, p.m, p.ldx, BK)) return rc;
+  }
+  if (int rc = make_map(&mAa, A, p.m, p.m, p.lda, BM)) return rc;
+  if (int rc = make_map(&mAb, A, p.m, p.m, p.lda, BN)) return rc;
+  if (int rc = make_map(&mBa, B, p.m, p.m, p.lda, BM)) return rc;
+
+  int cur = 0;
+  for (int it = 0; it < steps; ++it) {
+    const int nxt = cur ^ 1;
+    // A = X X^T
+    GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status, kSymmetric, 0};
+    if (int rc = gemm(false, mXa[cur], mXb[cur], g1, s)) return rc;
+    // B = c (A A^T) + b A   (A symmetric)
+    GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric, 0};
+    if (int rc = gemm(false, mAa, mAb, g2, s)) return rc;
+    // X' = B X + a X
+    GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0, 0};
+    if (int rc = gemm(true, mBa, mXmn[cur], g3, s)) return rc;
+    cur = nxt;
+  }
+  // y = X (transposed back for a tall input)
+  const dim3 og(unsigned((p.n + kCopyTile - 1) / kCopyTile), unsigned((p.m + kCopyTile - 1) / kCopyTile));
+  k_scale_copy<<<og, 256, 0, s>>>(Xs[cur], p.m, p.n, p.ldx, y, t.ld_y, p.tall ? 1 : 0, nullptr);
+  return check("bq_muon_ns (copy out)");
+}
+
+// The library's own side streams of the current device, forked from and joined
+// back to the caller's stream so that independent matrices of a batch fill one
+// another's idle SMs (the last wave of one matrix's product leaves SMs that the
+// next matrix's products use).  Created once per device; NULL when unavailable.
+constexpr int kNsStreams = 3;
+struct SidePool {
+  cudaStream_t st[kNsStreams];
+  cudaEvent_t fork, join[kNsStreams];
+  std::mutex mu;  // one batch at a time enqueues on the pool
+  bool ok = false;
+};
+
+SidePool* side_pool() {
+  static std::mutex mu;
+  static SidePool* pools[64] = {};
+  static bool tried[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!tried[dev]) {
+    tried[dev] = true;
+    auto* p = new SidePool();
+    bool ok = cudaEventCreateWithFlags(&p->fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int j = 0; ok && j < kNsStreams; ++j)
+      ok = cudaStreamCreateWithFlags(&p->st[j], cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&p->join[j], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      delete p;  // the handles already made stay with the context; the batch runs in order instead
+      return nullptr;
+    }
+    p->ok = true;
+    pools[dev] = p;
+  }
+  return pools[dev];
+}
+
+int run_batch(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws,
+              size_t ws_bytes, void* stream, bool allow_side) {
   if (batch < 0 || (batch > 0 && !mats) || steps < 0) return set_error(BQ_EINVAL, "bq_muon_ns: bad arguments");
   if (batch > 0 && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)))
     return set_error(BQ_EALIGN, "bq_muon_ns: workspace must be 256-byte aligned");
@@ -625,67 +717,62 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
     if (int rc = check_mat(mats[i])) return rc;
     if (ws_bytes < ns_plan(mats[i]).bytes) return set_error(BQ_ENOSPC, "bq_muon_ns: workspace too small");
   }
-  // the device error word sits at the same offset for every matrix; it is
-  // cleared once per call, so a wait that gave up on any matrix of the batch
-  // stays recorded (report() keeps the first site) until the next call
-  if (batch > 0 &&
-      cudaMemsetAsync(static_cast<unsigned char*>(ws) + kStatusOffset, 0, sizeof(int), s) != cudaSuccess)
-    return check("bq_muon_ns (status)");
+  if (batch == 0) return BQ_OK;
+  auto* w = static_cast<unsigned char*>(ws);
+  int* status = reinterpret_cast<int*>(w + kStatusOffset);
+  // the device error word is cleared once per call, so a wait that gave up on
+  // any matrix of the batch stays recorded (report() keeps the first site)
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return check("bq_muon_ns (status)");
+  std::vector<size_t> off;
+  const size_t conc = concurrent_bytes(batch, mats, &off);
+  SidePool* pool = (allow_side && batch > 1 && ws_bytes >= conc) ? side_pool() : nullptr;
+  if (!pool) {  // one matrix after another on the caller's stream, one region reused
+    for (int i = 0; i < batch; ++i)
+      if (int rc = ns_one(mats[i], w, status, steps, a, b, c, eps, s)) return rc;
+    return BQ_OK;
+  }
+  // matrices on the side streams, largest first to the least loaded stream
+  std::lock_guard<std::mutex> lock(pool->mu);
+  std::vector<int> order(static_cast<size_t>(batch));
+  std::vector<double> cost(static_cast<size_t>(batch));
   for (int i = 0; i < batch; ++i) {
-    const bq_mat& t = mats[i];
-    const NsPlan p = ns_plan(t);
-    auto* w = static_cast<unsigned char*>(ws);
-    float* part = reinterpret_cast<float*>(w + p.off_part);
-    int* status = reinterpret_cast<int*>(w + p.off_status);
-    float* inv = reinterpret_cast<float*>(w + p.off_status + 16);  // 1 / (||x||_F + eps)
-    auto* X0 = reinterpret_cast<__nv_bfloat16*>(w + p.off_x0);
-    auto* X1 = reinterpret_cast<__nv_bfloat16*>(w + p.off_x1);
-    auto* A = reinterpret_cast<__nv_bfloat16*>(w + p.off_a);
-    auto* B = reinterpret_cast<__nv_bfloat16*>(w + p.off_b);
-    const auto* x = static_cast<const __nv_bfloat16*>(t.x);
-    auto* y = static_cast<__nv_bfloat16*>(t.y);
-
-    // normalise into X0 (transposed for a tall input)
-    k_sumsq<<<kRedBlocks, kRedThreads, 0, s>>>(x, t.rows, t.cols, t.ld_x, part);
-    if (int rc = check("bq_muon_ns (norm)")) return rc;
-    const dim3 cg(unsigned((t.cols + kCopyTile - 1) / kCopyTile), unsigned((t.rows + kCopyTile - 1) / kCopyTile));
-    k_inv_norm<<<1, kRedThreads, 0, s>>>(part, kRedBlocks, eps, inv);
-    if (int rc = check("bq_muon_ns (inv norm)")) return rc;
-    k_scale_copy<<<cg, 256, 0, s>>>(x, t.rows, t.cols, t.ld_x, X0, p.ldx, p.tall ? 1 : 0, inv);
-    if (int rc = check("bq_muon_ns (scale)")) return rc;
-
-    // tensor maps: X as K-major A operand / K-major B operand / MN-major B operand, A, B
-    CUtensorMap mXa[2], mXb[2], mXmn[2], mAa, mAb, mBa;
-    __nv_bfloat16* Xs[2] = {X0, X1};
-    for (int j = 0; j < 2; ++j) {
-      if (int rc = make_map(&mXa[j], Xs[j], p.n, p.m, p.ldx, BM)) return rc;
-      if (int rc = make_map(&mXb[j], Xs[j], p.n, p.m, p.ldx, BN)) return rc;
-      if (int rc = make_map(&mXmn[j], Xs[j], p.n, p.m, p.ldx, BK)) return rc;
-    }
-    if (int rc = make_map(&mAa, A, p.m, p.m, p.lda, BM)) return rc;
-    if (int rc = make_map(&mAb, A, p.m, p.m, p.lda, BN)) return rc;
-    if (int rc = make_map(&mBa, B, p.m, p.m, p.lda, BM)) return rc;
-
-    int cur = 0;
-    for (int it = 0; it < steps; ++it) {
-      const int nxt = cur ^ 1;
-      // A = X X^T
-      GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status, kSymmetric, 0};
-      if (int rc = gemm(false, mXa[cur], mXb[cur], g1, s)) return rc;
-      // B = c (A A^T) + b A   (A symmetric)
-      GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric, 0};
-      if (int rc = gemm(false, mAa, mAb, g2, s)) return rc;
-      // X' = B X + a X
-      GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0, 0};
-      if (int rc = gemm(true, mBa, mXmn[cur], g3, s)) return rc;
-      cur = nxt;
-    }
-    // y = X (transposed back for a tall input)
-    const dim3 og(unsigned((p.n + kCopyTile - 1) / kCopyTile), unsigned((p.m + kCopyTile - 1) / kCopyTile));
-    k_scale_copy<<<og, 256, 0, s>>>(Xs[cur], p.m, p.n, p.ldx, y, t.ld_y, p.tall ? 1 : 0, nullptr);
-    if (int rc = check("bq_muon_ns (copy out)")) return rc;
+    const double m = double(std::min(mats[i].rows, mats[i].cols)), n = double(std::max(mats[i].rows, mats[i].cols));
+    cost[size_t(i)] = 4 * m * m * n + 2 * m * m * m;
+    order[size_t(i)] = i;
+  }
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[size_t(x)] > cost[size_t(y)]; });
+  double load[kNsStreams] = {};
+  if (cudaEventRecord(pool->fork, s) != cudaSuccess) return check("bq_muon_ns (fork)");
+  for (int j = 0; j < kNsStreams; ++j)
+    if (cudaStreamWaitEvent(pool->st[j], pool->fork, 0) != cudaSuccess) return check("bq_muon_ns (fork)");
+  for (int i : order) {
+    int j = 0;
+    for (int k = 1; k < kNsStreams; ++k)
+      if (load[k] < load[j]) j = k;
+    load[j] += cost[size_t(i)];
+    if (int rc = ns_one(mats[i], w + off[size_t(i)], status, steps, a, b, c, eps, pool->st[j])) return rc;
+  }
+  for (int j = 0; j < kNsStreams; ++j) {  // join every stream that waited on the fork
+    if (cudaEventRecord(pool->join[j], pool->st[j]) != cudaSuccess ||
+        cudaStreamWaitEvent(s, pool->join[j], 0) != cudaSuccess)
+      return check("bq_muon_ns (join)");
   }
   return BQ_OK;
+}
+
+}  // namespace
+
+int muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes) {
+  if (!bytes || batch < 0 || (batch > 0 && !mats)) return set_error(BQ_EINVAL, "bq_muon_ns_workspace: bad arguments");
+  for (int i = 0; i < batch; ++i)
+    if (int rc = check_mat(mats[i])) return rc;
+  *bytes = concurrent_bytes(batch, mats, nullptr);
+  return BQ_OK;
+}
+
+int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws, size_t ws_bytes,
+            void* stream) {
+  return run_batch(batch, mats, steps, a, b, c, eps, ws, ws_bytes, stream, true);
 }
 
 // ---------------------------------------------------------------- allocation-free variant
@@ -724,13 +811,17 @@ int static_scratch(void** out) {
 int muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* stream) {
   void* scratch = nullptr;
   if (int rc = static_scratch(&scratch)) return rc;
-  size_t need = 0;
-  if (int rc = muon_ns_workspace(batch, mats, &need)) return rc;
+  if (batch < 0 || (batch > 0 && !mats)) return set_error(BQ_EINVAL, "bq_muon_ns_noalloc: bad arguments");
+  size_t need = 256;  // the matrices run one after another and reuse one region
+  for (int i = 0; i < batch; ++i) {
+    if (int rc = check_mat(mats[i])) return rc;
+    need = std::max(need, ns_plan(mats[i]).bytes);
+  }
   if (need > kStaticScratchBytes)
     return set_error(BQ_ENOSPC, "bq_muon_ns_noalloc: the batch needs " + std::to_string(need) +
                                     " bytes of scratch; the static scratch holds " +
                                     std::to_string(kStaticScratchBytes) + " (use bq_muon_ns with a workspace)");
-  return muon_ns(batch, mats, steps, a, b, c, eps, scratch, kStaticScratchBytes, stream);
+  return run_batch(batch, mats, steps, a, b, c, eps, scratch, kStaticScratchBytes, stream, false);
 }
 
 // ws == NULL: the static scratch of the current device (bq_muon_ns_noalloc)

@@ -279,8 +279,16 @@ int bq_quant_fp8(const bq_shard* shard, const float* master, uint8_t* fp8_out, f
  * on tcgen05 tensor cores: bf16 operands, fp32 accumulation, bf16 storage of
  * X, A, B between products, fp32 Frobenius norm.
  * mats: host array; ws: device workspace of ws_bytes, 256-byte aligned (bf16
- * scratch for X, A, B, fp32 partial norms and an error word), size from
- * bq_muon_ns_workspace; matrices are processed one after another and reuse it.
+ * scratch for X, A, B, fp32 partial norms and an error word).
+ * bq_muon_ns_workspace gives the size that lets the matrices of a batch run
+ * concurrently: each gets its own region and the library forks them onto its
+ * own side streams (three per device, created on the first such call, never
+ * destroyed) from `stream` and joins them back into it, so the idle SMs of one
+ * matrix's products run another's (an ordinary fork and join of events, which
+ * also works inside a stream capture; one batch at a time enqueues on a
+ * device's side streams).  Any ws_bytes of at least the largest single
+ * matrix's need also works: the matrices then run one after another on
+ * `stream` and reuse one region.  The results are the same either way.
  * Errors: BQ_EINVAL (bad descriptor, rows or cols above 2^20), BQ_EALIGN,
  * BQ_ENOSPC, BQ_EDEVICE (driver entry point for tensor maps unavailable). */
 int bq_muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes);
@@ -362,7 +370,8 @@ int bq_muon_apply(const bq_shard* shard, float* master, const void* const* updat
  * The caller passes inputs and outputs as for bq_muon_ns; the scratch is a fixed
  * 32 MiB array inside the library's device image (every GPU that loads the
  * library holds it until the process exits), so nothing is allocated and no
- * workspace is passed.  A batch whose bq_muon_ns_workspace size exceeds 32 MiB
+ * workspace is passed.  The matrices run one after another on `stream` (no side
+ * streams), reusing the scratch; a batch with a matrix needing more than 32 MiB
  * is rejected with BQ_ENOSPC before any work is queued (for example, a 1024 x
  * 4096 matrix fits; a 2048 x 2048 one does not).
  * The first call on each device looks up the scratch array's device address
