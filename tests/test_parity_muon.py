@@ -61,3 +61,52 @@ def test_degenerate_inputs(cuda):
     assert not torch.isnan(y).any() and int(torch.count_nonzero(y)) == 0
     errs = run_muon_case(cuda, [(1, 64), (64, 1), (8, 8), (3, 1000)], steps=5)
     assert max(errs) < TOL, errs
+
+
+def test_concurrent_sequential_and_graphed_batches_agree(cuda):
+    """A batch with the full workspace runs its matrices concurrently on the
+    library's side streams; with only the largest matrix's need it runs them one
+    after another; captured in a CUDA graph the fork and join become graph
+    edges.  The kernels are the same, so all three give the same bits, and each
+    is within the tolerance of the fp64 oracle."""
+    import torch
+
+    import block_quant_gb300 as bq
+    from oracle import muon as OM
+
+    shapes = [(256, 640), (384, 384), (640, 200), (128, 1000)]
+    bits = [W.muon_input_bits(61, i, r, c) for i, (r, c) in enumerate(shapes)]
+    xs = [torch.from_numpy(b.view(np.int16)).to(cuda).view(torch.bfloat16) for b in bits]
+
+    def batch():
+        ys = [torch.full_like(x, float("nan")) for x in xs]
+        return ys, [(x, y, r, c) for x, y, (r, c) in zip(xs, ys, shapes)]
+
+    y_conc, mats = batch()
+    full = bq.muon_ns_workspace(mats)
+    single = max(bq.muon_ns_workspace([m]) for m in mats)
+    assert full > single
+    ws = torch.empty(full, dtype=torch.uint8, device=cuda)
+    bq.muon_ns(mats, ws)
+    bq.muon_ns_check(ws)
+    y_seq, mats_s = batch()
+    bq.muon_ns(mats_s, ws, ws_bytes=single)
+    bq.muon_ns_check(ws)
+    y_graph, mats_g = batch()
+    side = torch.cuda.Stream(cuda)
+    torch.cuda.synchronize(cuda)
+    with torch.cuda.stream(side):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            bq.muon_ns(mats_g, ws, stream=side)
+        g.replay()
+    torch.cuda.synchronize(cuda)
+    bq.muon_ns_check(ws)
+    for (r, c), b, a, s_, gr in zip(shapes, bits, y_conc, y_seq, y_graph):
+        ai = a.view(torch.int16).cpu().numpy()
+        assert np.array_equal(ai, s_.view(torch.int16).cpu().numpy()), (r, c, "sequential")
+        assert np.array_equal(ai, gr.view(torch.int16).cpu().numpy()), (r, c, "graph")
+        x64 = (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ref = OM.newton_schulz(x64, steps=5)
+        got = a.float().cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < TOL, (r, c)
