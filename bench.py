@@ -285,24 +285,31 @@ class GroupStep:
         self.dbuf = torch.empty(E, dtype=torch.bfloat16, device=dev)
         self.fp8 = torch.zeros(E, dtype=torch.uint8, device=dev)
         self.fs = torch.zeros(nf, dtype=torch.float32, device=dev)
-        # every member's gradients over its owned ranges (distinct allocations)
+        # every member's gradients over their owned ranges: distinct tensors (no
+        # two share an element), carved back to back out of one allocation so
+        # that a step's upload from the host is one copy
         self.grads, self.grad_lo = {}, {}
         ptrs = np.zeros(max(info["tensors"], 1), np.int64)
         self.bytes = dict(elems=0, pads=0, pack=0, adam=0, total=0, adam_blocks=0, fp8_tiles=0, fp8_elems=0)
-        kinds, covered = set(), 0
+        kinds, covered, spans, nG = set(), 0, [], 0
         for u, p in zip(mem, self.group.place):
             T = tables[u]
             for i in range(T.N):
                 a, b = T.owned_range(i, lo, hi)
                 if b > a:
-                    gi = p["tensor_base"] + i
-                    self.grads[gi] = (torch.randn(b - a, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
-                    self.grad_lo[gi] = a
-                    ptrs[gi] = self.grads[gi].data_ptr() - 2 * a
+                    spans.append((p["tensor_base"] + i, nG, a, b - a))
+                    nG += -(-(b - a) // 8) * 8  # 16-byte aligned starts
             for k, v in step_bytes(T, lo, hi).items():
                 self.bytes[k] += v
             kinds |= adam_kinds(T, lo, hi)
             covered += (hi - lo) * T.S
+        self.gbuf = torch.empty(max(nG, 8), dtype=torch.bfloat16, device=dev)
+        _fill(self.gbuf, lambda k: (torch.randn(k, generator=g, device=dev) * 1e-3).to(torch.bfloat16))
+        self.grad_spans = spans
+        for gi, off, a, n in spans:
+            self.grads[gi] = self.gbuf[off:off + n]
+            self.grad_lo[gi] = a
+            ptrs[gi] = self.grads[gi].data_ptr() - 2 * a
         gaps = E - covered  # alignment gaps between members: padding, zeroed by the pack
         self.bytes["pads"] += gaps
         self.bytes["pack"] += 2 * gaps
@@ -344,19 +351,19 @@ class E2EPipeline:
     def __init__(self, step, dev):
         torch = self.torch = step.torch
         self.step, self.bq = step, step.bq
-        self.host_grads = {i: torch.empty(g.numel(), dtype=torch.bfloat16, pin_memory=True)
-                           for i, g in step.grads.items()}
-        for i, g in step.grads.items():
-            self.host_grads[i].copy_(g)
+        # one pinned host buffer with every gradient at its offset in the
+        # device's gradient allocation: one upload per step
+        self.host_grads = torch.empty(step.gbuf.numel(), dtype=torch.bfloat16, pin_memory=True)
+        self.host_grads.copy_(step.gbuf)
         self.host_fp8 = torch.empty(step.fp8.numel(), dtype=torch.uint8, pin_memory=True)
         self.host_fs = torch.empty(step.fs.numel(), dtype=torch.float32, pin_memory=True)
-        self.h2d = sum(g.numel() * 2 for g in step.grads.values())
+        self.h2d = step.gbuf.numel() * 2
         self.d2h = step.fp8.numel() + step.fs.numel() * 4
-        second, ptrs = {}, np.zeros(len(step.gptrs), np.int64)
-        for i, g in step.grads.items():
-            second[i] = torch.empty_like(g)
-            ptrs[i] = second[i].data_ptr() - 2 * step.grad_lo[i]
-        self.gsets = [step.grads, second]
+        second = torch.empty_like(step.gbuf)
+        ptrs = np.zeros(len(step.gptrs), np.int64)
+        for gi, off, a, n in step.grad_spans:
+            ptrs[gi] = second[off:off + n].data_ptr() - 2 * a
+        self.gbufs = [step.gbuf, second]
         self.gptrs = [step.gptrs, torch.from_numpy(ptrs).to(dev)]
         self.fp8 = [step.fp8, torch.empty_like(step.fp8)]
         self.fs = [step.fs, torch.empty_like(step.fs)]
@@ -369,8 +376,7 @@ class E2EPipeline:
         st, torch, j = self.step, self.torch, self.k & 1
         self.up.wait_event(self.ev_packed[j])  # the pack two steps back has read this set
         with torch.cuda.stream(self.up):
-            for i, g in self.gsets[j].items():
-                g.copy_(self.host_grads[i], non_blocking=True)
+            self.gbufs[j].copy_(self.host_grads, non_blocking=True)
             self.ev_up[j].record(self.up)
         comp.wait_event(self.ev_up[j])
         st.pack(comp, gptrs=self.gptrs[j])
