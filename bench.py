@@ -44,6 +44,12 @@ GPTOSS = "gpt-oss-120b-rank0"
 MUON = "muon-ns"
 L2_BYTES = 126 * 2 ** 20
 GROUP_ALIGN = 256  # elements between group members' bases (the library's member alignment)
+ROOFLINE_KERNEL = {
+    WORKLOAD: "bq_step_adam8 on the group (k_tile: 128x128 Adam tiles + fused FP8; k_flat<4>: the 1-D norms)",
+    LAYER: "bq_step_adam8 (k_strip: 256-element Adam blocks + fused 128x128 FP8; k_flat<8>: the norms)",
+    GPTOSS: "bq_step_adam8 on the group (k_strip over strips and band pieces, k_quant_region for the band FP8 "
+            "tiles, k_flat<8>)",
+}
 
 
 def peaks():
@@ -652,32 +658,41 @@ def cpu_info():
     return dict(cpu_model=model, cpu_count=os.cpu_count(), affinity=f"{len(aff)} cpus ({aff[0]}-{aff[-1]})")
 
 
-def cpu_baseline(single_seconds=8.0):
+def sample_unit(workload):
+    """The unit of a workload the CPU legs sample: its repeated layer unit, else its first."""
+    units = W.config(workload).units
+    return max(range(len(units)), key=lambda u: (units[u].repeat, -u))
+
+
+def cpu_baseline(workload=WORKLOAD, single_seconds=8.0):
     """The oracle as it stands, timed on the host cores on a bounded sample of the
-    benchmarked workload: the Llama-3-70B layer unit's slice on one device
-    (14.7 M elements, its own seeded inputs), through the oracle's pack, 8-bit
-    Adam and FP8.  Two legs: one core, the slice repeated for about
-    single_seconds; all cores, one slice per worker process (spawned; workers
-    independent, as the blocks are), aggregate = sum of the workers' rates."""
+    benchmarked workload: its layer unit's slice on one device (for the
+    Llama-3-70B slice 13.6 M elements, its own seeded inputs), through the
+    oracle's pack, 8-bit Adam and FP8.  Two legs: one core, the slice repeated
+    for about single_seconds; all cores, one slice per worker process (spawned;
+    workers independent, as the blocks are), aggregate = sum of the workers'
+    rates."""
     import multiprocessing as mp
 
     info = cpu_info()
-    b, e, t = _oracle_slice((WORKLOAD, 1, 0, 1))
+    u = sample_unit(workload)
+    cfg = W.config(workload)
+    V, d0 = cfg.V, cfg.dev_lo
+    b, e, t = _oracle_slice((workload, u, d0, 1))
     reps = max(1, int(round(single_seconds / max(t, 1e-3))) - 1)
-    b2, e2, t2 = _oracle_slice((WORKLOAD, 1, 0, reps)) if reps > 0 else (0, 0, 0.0)
+    b2, e2, t2 = _oracle_slice((workload, u, d0, reps)) if reps > 0 else (0, 0, 0.0)
     one = (b + b2) / (t + t2) / 1e9
     n1 = 1 + reps
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
-    V = W.config(WORKLOAD).V
     ctx = mp.get_context("spawn")
     t0 = time.perf_counter()
     with ctx.Pool(cores) as pool:
-        res = pool.map(_oracle_slice, [(WORKLOAD, 1, k % V, 1) for k in range(cores)])
+        res = pool.map(_oracle_slice, [(workload, u, k % V, 1) for k in range(cores)])
     wall = time.perf_counter() - t0
     agg = sum(bb / tt for bb, _, tt in res) / 1e9
     return {"value": round(agg, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"the llama3-70b layer unit's slice on one device of V=64 ({e} elements, seeded workload "
-                      f"inputs): oracle pack + 8-bit Adam (128x128 tiles) + FP8, numpy; {cores} spawned worker "
+            "sample": f"the {workload} {cfg.units[u].name} unit's slice on one device of V={V} ({e} elements, "
+                      f"seeded workload inputs): oracle pack + 8-bit Adam + FP8, numpy; {cores} spawned worker "
                       f"processes, one slice each (devices 0..{min(cores, V) - 1}), aggregate of the workers' "
                       f"rates ({wall:.1f} s wall with input generation)",
             "single_core": {"value": round(one, 4), "unit": "GB/s", "cores": 1,
@@ -739,9 +754,11 @@ def run_ours(args):
     import block_quant_gb300 as bq
 
     bq.load()
-    V = W.config(WORKLOAD).V
-    # rank r steps device r's shard of every unit (weak scaling, no collective)
-    step = GroupStep(WORKLOAD, dev, seed=1000 + rank, dev_lo=rank % V, members=args.members)
+    cfg = W.config(args.workload)
+    # rank r steps device r's shard of every unit of a one-device slice (weak
+    # scaling, no collective); a whole-buffer workload is stepped whole by every rank
+    lo = rank % cfg.V if cfg.dev_hi - cfg.dev_lo == 1 else cfg.dev_lo
+    step = GroupStep(args.workload, dev, seed=1000 + rank, dev_lo=lo, members=args.members)
     muon = MuonBatch(W.config(MUON).muon_shapes, dev, seed=2000 + rank) if args.muon else None
     stream = torch.cuda.current_stream(dev)
 
@@ -821,6 +838,8 @@ def run_ours(args):
         # the other configurations, each stepped as a group of its own
         for name, key in ((LAYER, "llama3_8b_layer"), (GPTOSS, "gpt_oss_120b_rank0"),
                           ("llama3-8b-layer-tile32", "adam_tile32"), ("toy", "toy_step")):
+            if name == args.workload:
+                continue
             cfgV = W.config(name).V
             lo = 0 if name in (LAYER, "llama3-8b-layer-tile32", "toy") else rank % cfgV
             st = GroupStep(name, dev, seed=4000 + rank, dev_lo=lo)
@@ -856,10 +875,10 @@ def run_ours(args):
                      "GB/s": round(gbs(head["bytes"]["pack"], statistics.mean(pack_ms)), 1),
                      "bytes": head["bytes"]["pack"]},
             "roofline": {"bound": "hbm",
-                         "kernel": "bq_step_adam8 on the group (k_tile: 128x128 Adam tiles + fused FP8; "
-                                   "k_flat<4>: the 1-D norms)",
+                         "kernel": ROOFLINE_KERNEL[args.workload],
                          "achieved": round(adam_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                         "frac": round(adam_gbs / pk["hbm"], 4), "traffic": recorded_traffic("bq_step_adam8"),
+                         "frac": round(adam_gbs / pk["hbm"], 4),
+                         "traffic": recorded_traffic("bq_step_adam8") if args.workload == WORKLOAD else None,
                          "peak_source": f"{pk['src']} hbm_gbs (STREAM-style copy)",
                          "ms": round(adam_max, 4), "algorithmic_bytes": head["bytes"]["adam"],
                          "launches_per_call": head["launches"] - 1},
@@ -946,7 +965,7 @@ def run_ours(args):
                 "root_ns_tflop_per_device": ms_obj.root_tflop,
                 "note": "measured after the timed region; not part of value"}
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(args.workload)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -975,7 +994,7 @@ def reference_config(args, world):
     arm runs no library code) and the same member alignment."""
     from oracle import planner as OP
 
-    cfg = W.config(WORKLOAD)
+    cfg = W.config(args.workload)
     lo, hi = cfg.dev_lo, cfg.dev_hi
     tot = {k: 0 for k in ("elems", "pads", "pack", "adam", "total", "adam_blocks", "fp8_tiles", "fp8_elems")}
     S, end, covered = {}, 0, 0
@@ -1000,8 +1019,8 @@ def reference_config(args, world):
     tot["pack"] += 2 * gaps
     tot["total"] += 2 * gaps
     units = ", ".join(f"{u.name} x{u.repeat}" if u.repeat > 1 else u.name for u in cfg.units)
-    describe = (f"{WORKLOAD}: local shard {lo}..{hi - 1} of V={cfg.V} of every unit ({units}; {len(mem)} members) "
-                f"in one group")
+    describe = (f"{args.workload}: local shard{'s' if hi - lo > 1 else ''} {lo}..{hi - 1} of V={cfg.V} of every "
+                f"unit ({units}; {len(mem)} members) in one group")
     return workload_config(describe, tot, S, end, len(mem), args.muon, world)
 
 
@@ -1013,9 +1032,10 @@ def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
+    u, d0 = sample_unit(args.workload), W.config(args.workload).dev_lo
     for _ in range(args.warmup):
-        _oracle_slice((WORKLOAD, 1, 0, 1))
-    res = [_oracle_slice((WORKLOAD, 1, 0, 1)) for _ in range(args.steps)]
+        _oracle_slice((args.workload, u, d0, 1))
+    res = [_oracle_slice((args.workload, u, d0, 1)) for _ in range(args.steps)]
     v = sum(b for b, _, _ in res) / sum(t for _, _, t in res) / 1e9
     ms = 1e3 * statistics.mean(t for _, _, t in res)
     line = {
@@ -1024,8 +1044,9 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
         "config": reference_config(args, world),
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"per step the llama3-70b layer unit's slice on device 0 ({res[0][1]} elements, "
-                                   "seeded workload inputs) through the oracle's pack, 8-bit Adam and FP8 on one core",
+                         "sample": f"per step the {args.workload} {W.config(args.workload).units[u].name} unit's "
+                                   f"slice on device {d0} ({res[0][1]} elements, seeded workload inputs) through the "
+                                   "oracle's pack, 8-bit Adam and FP8 on one core",
                          **cpu_info()},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -1047,6 +1068,8 @@ def main():
     ap.add_argument("--no-dequant", dest="dequant", action="store_false")
     ap.add_argument("--muon-step", dest="muon_step", action="store_true", default=True)
     ap.add_argument("--no-muon-step", dest="muon_step", action="store_false")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, LAYER, GPTOSS],
+                    help="the DBuffer step benchmarked (default: the Llama-3-70B rank-0 slice)")
     ap.add_argument("--members", type=int, default=None,
                     help="step only the first K members of the group (smaller case for profiling)")
     args = ap.parse_args()

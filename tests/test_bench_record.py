@@ -35,7 +35,7 @@ def test_reference_config_matches_library_group():
     import block_quant_gb300 as bq
     import workloads as W
 
-    args = argparse.Namespace(members=None, muon=True)
+    args = argparse.Namespace(members=None, muon=True, workload=bench.WORKLOAD)
     ref = bench.reference_config(args, 1)
     cfg = W.config(bench.WORKLOAD)
     lays = [bq.plan(u.tensors, cfg.V, cfg.alpha, cfg.start_align) for u in cfg.units]
