@@ -14,8 +14,12 @@ planner   RaggedShard layout problem: earliest-fit feasibility, the prefix /
 codecs    bf16 round-to-nearest-even, OCP FP8 E4M3 encode/decode, linear absmax
           int8 / uint8 block quantisers.
 pack      group-level pre-communication add / scale / zero / copy into the DBuffer.
-adam8     block-wise 8-bit Adam step (dequantise, fp32 update, requantise).
-fp8       128x128 block FP8 requantisation of the updated parameters.
+adam8     block-wise 8-bit Adam step (dequantise, fp32 update, requantise), in the
+          operation order the kernels reproduce bit for bit (the contract leg).
+fp8       128x128 block FP8 requantisation of the updated parameters (contract leg).
+plain     the same Adam step and FP8 requantisation in the plainest operation order
+          (every fp32 operation separate, division by the scales and the bias
+          corrections): the textbook definition the kernels are measured against.
 muon      Newton-Schulz orthogonalisation in fp64.
 
 Sources (cited per function): "veScale-FSDP: Flexible and High-Performance FSDP at
@@ -28,4 +32,4 @@ Parity status: every function here is pinned by ``tests/test_oracle_*.py`` again
 brute force, closed forms or a library routine; none is "parity unpinned".
 """
 
-from . import codecs, planner, pack, adam8, fp8, muon  # noqa: F401
+from . import codecs, planner, pack, adam8, fp8, muon, plain  # noqa: F401
