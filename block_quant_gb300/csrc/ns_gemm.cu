@@ -745,19 +745,21 @@ int run_batch(int batch, const bq_mat* mats, int steps, float a, float b, float 
   if (cudaEventRecord(pool->fork, s) != cudaSuccess) return check("bq_muon_ns (fork)");
   for (int j = 0; j < kNsStreams; ++j)
     if (cudaStreamWaitEvent(pool->st[j], pool->fork, 0) != cudaSuccess) return check("bq_muon_ns (fork)");
+  int rc = BQ_OK;
   for (int i : order) {
     int j = 0;
     for (int k = 1; k < kNsStreams; ++k)
       if (load[k] < load[j]) j = k;
     load[j] += cost[size_t(i)];
-    if (int rc = ns_one(mats[i], w + off[size_t(i)], status, steps, a, b, c, eps, pool->st[j])) return rc;
+    rc = ns_one(mats[i], w + off[size_t(i)], status, steps, a, b, c, eps, pool->st[j]);
+    if (rc != BQ_OK) break;  // what was queued is still joined below
   }
   for (int j = 0; j < kNsStreams; ++j) {  // join every stream that waited on the fork
     if (cudaEventRecord(pool->join[j], pool->st[j]) != cudaSuccess ||
         cudaStreamWaitEvent(s, pool->join[j], 0) != cudaSuccess)
-      return check("bq_muon_ns (join)");
+      return rc != BQ_OK ? rc : check("bq_muon_ns (join)");
   }
-  return BQ_OK;
+  return rc;
 }
 
 }  // namespace
