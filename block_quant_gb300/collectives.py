@@ -14,10 +14,18 @@ slices of caller buffers:
     per rank: exchanged padded to the longest rank, then trimmed).
 
 Ranks own equal runs of consecutive devices: rank r of W owns devices
-[r*V/W, (r+1)*V/W) (V % W == 0).  Nothing here computes any of the method's
-arithmetic: the reduction is the collective's sum, everything else moves bytes.
-The calls are torch.distributed collectives on the caller's tensors (NCCL on
-GPUs; tested on CPU ranks over gloo).
+[r*V/W, (r+1)*V/W) (V % W == 0).
+
+The n-D DBuffer (same passage: a DBuffer sharded over one mesh dimension and
+replicated over another) adds one exchange: on a mesh of R replicas x W shards
+(rank = replica * W + shard), the ReduceScatter runs inside each replica's shard
+group and an AllReduce of the reduced slice runs across the replicas holding the
+same shard; the AllGather stays inside the shard group.
+
+Nothing here computes any of the method's arithmetic: the reduction is the
+collective's sum, everything else moves bytes.  The calls are torch.distributed
+collectives on the caller's tensors (NCCL on GPUs; tested on CPU ranks over
+gloo).
 """
 
 import numpy as np
@@ -29,6 +37,36 @@ def rank_devices(V, world, rank):
         raise ValueError(f"need V % world == 0 and 0 <= rank < world (V={V}, world={world}, rank={rank})")
     k = V // world
     return rank * k, (rank + 1) * k
+
+
+def mesh_groups(replicas, shards):
+    """The process groups of a replicas x shards mesh (rank = replica * shards +
+    shard): this rank's shard group (the ranks of its replica) and replica group
+    (the ranks holding its shard), created collectively on every rank."""
+    import torch.distributed as dist
+
+    rank = dist.get_rank()
+    if dist.get_world_size() != replicas * shards:
+        raise ValueError("the world is not replicas x shards")
+    shard_group = replica_group = None
+    for r in range(replicas):  # every rank creates every group, in the same order
+        g = dist.new_group([r * shards + s for s in range(shards)])
+        if rank // shards == r:
+            shard_group = g
+    for s in range(shards):
+        g = dist.new_group([r * shards + s for r in range(replicas)])
+        if rank % shards == s:
+            replica_group = g
+    return shard_group, replica_group
+
+
+def reduce_scatter_allreduce_grad(full, local, shard_group, replica_group):
+    """n-D DBuffer: local <- this rank's slice summed over its shard group, then
+    summed over its replica group (in place)."""
+    import torch.distributed as dist
+
+    reduce_scatter_grad(full, local, group=shard_group)
+    dist.all_reduce(local, op=dist.ReduceOp.SUM, group=replica_group)
 
 
 def device_table(layout):

@@ -1,4 +1,5 @@
-"""The exchanges around the DBuffer step on CPU ranks (world_size 2 over gloo).
+"""The exchanges around the DBuffer step on CPU ranks over gloo (world_size 2, and
+a 2 x 2 replicas x shards mesh for the n-D DBuffer).
 
 Each rank packs its own gradients into the whole DBuffer (all V devices), the
 ReduceScatter gives it the summed slice of its own devices, it runs the step
@@ -171,3 +172,84 @@ def test_rank_devices_and_device_table():
     lay = bq.plan(c.units[0].tensors, c.V, c.alpha, c.start_align)
     T = W.Table(lay.export())
     assert np.array_equal(X.device_table(lay), T.devices)
+
+
+def _mesh_worker(rank, world, port, name, replicas, q):
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch
+    import torch.distributed as dist
+
+    import workloads as W
+    from block_quant_gb300 import collectives as X
+    from oracle import pack as OP
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        shards = world // replicas
+        sg, rg = X.mesh_groups(replicas, shards)
+        c, olay, lay, grads = _inputs(name, rank)
+        T = W.Table(lay.export())
+        V, S = c.V, T.S
+        lo, hi = X.rank_devices(V, shards, rank % shards)
+        full = OP.pack(olay, 0, V, grads, np.zeros(V * S, np.uint16), np.float32(1.0 / world), False)
+        t_local = torch.empty((hi - lo) * S, dtype=torch.bfloat16)
+        X.reduce_scatter_allreduce_grad(torch.from_numpy(full.view(np.int16)).view(torch.bfloat16), t_local, sg, rg)
+        local = t_local.view(torch.int16).numpy().view(np.uint16)
+        q8, fs, ms, vs = _step(c, olay, T, lo, hi, local)
+        t_q = torch.empty(V * S, dtype=torch.uint8)
+        X.all_gather_fp8(torch.from_numpy(q8), t_q, group=sg)
+        g_fs = torch.zeros(T.slot_range(0, V, fp8=True)[1])
+        X.all_gather_scales(lay, torch.from_numpy(fs), g_fs, fp8=True, group=sg)
+        q.put((rank, local, t_q.numpy(), g_fs.numpy(), None))
+    except Exception as e:  # reported to the parent, which fails the test
+        q.put((rank, None, None, None, repr(e)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_n_d_dbuffer_mesh_equals_the_v_shard_oracle():
+    """A 2 x 2 mesh (2 replicas x 2 shards): ReduceScatter inside the shard group,
+    AllReduce across the replicas, the step on the rank's devices, AllGather inside
+    the shard group.  Every rank ends with the FP8 buffer and scales of one process
+    running the oracle over all V devices on the same two-level sum."""
+    sys.path.insert(0, ROOT)
+    import workloads as W
+    from block_quant_gb300 import collectives as X
+    from oracle import codecs as OC
+    from oracle import pack as OP
+
+    name, world, replicas = "gptoss-small", 4, 2
+    shards = world // replicas
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _port()
+    procs = [ctx.Process(target=_mesh_worker, args=(r, world, port, name, replicas, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = {}
+    for _ in range(world):
+        r = q.get(timeout=600)
+        out[r[0]] = r[1:]
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for r, res in out.items():
+        assert res[-1] is None, f"rank {r}: {res[-1]}"
+    c, olay, lay, _ = _inputs(name, 0)
+    T = W.Table(lay.export())
+    V, S = c.V, T.S
+    sc = np.float32(1.0 / world)
+    packed = [OP.pack(olay, 0, V, _inputs(name, r)[3], np.zeros(V * S, np.uint16), sc, False) for r in range(world)]
+    f = OC.bf16_bits_to_f32
+    # the sum inside each replica's shard group, then across the replicas (each a single rounded add)
+    per_replica = [OC.f32_to_bf16_bits(f(packed[rr * shards]) + f(packed[rr * shards + 1])) for rr in range(replicas)]
+    summed = OC.f32_to_bf16_bits(f(per_replica[0]) + f(per_replica[1]))
+    for r in range(world):
+        lo, hi = X.rank_devices(V, shards, r % shards)
+        assert np.array_equal(out[r][0], summed[lo * S:hi * S]), f"rank {r}: reduced slice"
+    q8, fs, _, _ = _step(c, olay, T, 0, V, summed)
+    for r in range(world):
+        assert np.array_equal(out[r][1], q8), f"rank {r}: gathered FP8 codes"
+        assert np.array_equal(out[r][2].view(np.uint32), fs.view(np.uint32)), f"rank {r}: gathered FP8 scales"
