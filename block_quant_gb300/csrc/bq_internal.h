@@ -169,6 +169,6 @@ int muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, 
 int set_error(int code, const std::string& msg);
 int sm_count();  // SMs of the current device (cached per device)
 bool once_per_device(int key);  // true once per (current device, key); keys below
-constexpr int kOnceStripAttr = 0, kOnceGemmAttr = 1;
+constexpr int kOnceStripAttr = 0, kOnceGemmAttr = 1, kOnceTileAttr = 2;
 
 }  // namespace bq

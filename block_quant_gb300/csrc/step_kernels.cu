@@ -808,9 +808,9 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
 // ---------------------------------------------------------------- 128x128 Adam tiles (+ FP8 of the same tile)
 // Phase 1: Adam, write master, block-reduce max|m'|, max v', max|p'|; each
 // element's inputs (bf16 gradient, m code, v code) also go to tensor memory as
-// one packed 32-bit word.
+// one packed 32-bit word, and with FP8 its p' to shared memory (64 KB a tile).
 // Phase 2: requantise m', v' (recomputed bit-identically from those words and
-// the old scales held in registers) and convert p' (re-read, L2).
+// the old scales held in registers) and convert p' from shared memory.
 // Thread t handles the tile's vectors t + 256 i (i < 8, a tile has at most 2048
 // eight-element vectors); vector i's words live in the thread's TMEM lane (lane
 // quarter warp % 4) at columns 64 (warp / 4) + 8 i .. + 7: 128 columns per CTA.
@@ -850,6 +850,9 @@ template <bool FP8>
 __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
   __shared__ uint32_t red[3 * kWarps];
   __shared__ uint32_t s_tmem;
+  // FP8: the tile's p', thread t's vector i at float4 pair 2 (256 i + t): the
+  // second phase converts it from here instead of re-reading the master
+  extern __shared__ float4 s_p[];
   const int warp = threadIdx.x >> 5;
   if (warp == 0) tmem_alloc(smem_u32(&s_tmem), kTileTmemCols);
   tc_fence_before();
@@ -890,6 +893,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
       if (ok0) {
         adam_raw<true>(h, x0, 8, sm, sv, o);
         store_p8(a.master + pos0, o.p1);
+        if (fp8) store_p8(reinterpret_cast<float*>(s_p + 2 * (kThreads * i + int(threadIdx.x))), o.p1);
         am = max(am, o.am);
         av = max(av, o.av);
         ap = max(ap, o.ap);
@@ -897,6 +901,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
       if (ok1) {
         adam_raw<true>(h, x1, 8, sm, sv, o);
         store_p8(a.master + pos1, o.p1);
+        if (fp8) store_p8(reinterpret_cast<float*>(s_p + 2 * (kThreads * (i + 1) + int(threadIdx.x))), o.p1);
         am = max(am, o.am);
         av = max(av, o.av);
         ap = max(ap, o.ap);
@@ -936,15 +941,14 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
         adam_raw<true>(h, x, 8, sm, sv, o);
         *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);
         *reinterpret_cast<uint2*>(a.v + pos) = codes_uint8(o.v1, qv);
-        if (fp8) {  // the master words now hold p'
-          const float4 p0 = *reinterpret_cast<const float4*>(a.master + pos);
-          const float4 p1 = *reinterpret_cast<const float4*>(a.master + pos + 4);
+        if (fp8) {  // this thread's p' of vector v, kept in shared memory by the first phase
+          const float4 p0 = s_p[2 * v], p1 = s_p[2 * v + 1];
           const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
           *reinterpret_cast<uint2*>(a.fp8 + pos) = codes_e4m3(pv, qp);
         }
       }
     }
-    __syncthreads();  // red is reused by the next tile
+    __syncthreads();  // red and s_p are reused by the next tile
   }
   tc_fence_before();
   __syncthreads();  // every warp is done with TMEM before it is freed
@@ -1376,8 +1380,12 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
   }
   if (t.n_tiles) {
     const int grid = std::min(t.n_tiles, sms * kTileCtasPerSm);
+    constexpr int kTileP = 8 * kThreads * 2 * int(sizeof(float4));  // a 128x128 tile's p' (64 KB)
+    if (once_per_device(kOnceTileAttr) &&
+        cudaFuncSetAttribute(k_tile<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTileP) != cudaSuccess)
+      return check_launch("bq_step_adam8 (tile shared memory attribute)");
     if (fp8)
-      k_tile<true><<<grid, kThreads, 0, s>>>(t.tiles, t.n_tiles, a);
+      k_tile<true><<<grid, kThreads, kTileP, s>>>(t.tiles, t.n_tiles, a);
     else
       k_tile<false><<<grid, kThreads, 0, s>>>(t.tiles, t.n_tiles, a);
     if (int rc = check_launch("bq_step_adam8 (tiles)")) return rc;
