@@ -36,7 +36,7 @@ constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + 4 * 2560 /*mirror buffers*/;
 constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
 // X X^T and (A A^T with A symmetric) have symmetric results: compute the tiles
 // touching the upper triangle only and mirror them
@@ -144,19 +144,26 @@ struct GemmArgs {
 // Epilogue of one 128 x 256 tile: TMEM accumulator columns [col_base, col_base +
 // 256) -> alpha * acc + beta * C -> bf16 D (symmetric results: columns >= row
 // written directly, those > row mirrored).  Called by the four epilogue warps;
-// q = the TMEM lane quarter the warp may access.
+// q = the TMEM lane quarter the warp may access, lane = its row of the quarter.
+// The mirror goes through the warp's shared-memory buffer tb (32 rows of
+// kTbPitch bf16): the warp's 32 x 32 block is transposed there, so that each lane
+// writes one mirrored row of 32 elements with 16-byte stores.
+constexpr int kTbPitch = 40;  // bf16 per transposed row (80 bytes: 16-byte aligned rows)
+constexpr int kTbBytes = 32 * kTbPitch * 2;
+static_assert(kTbBytes == 2560, "the kernel reserves 2560 bytes of mirror buffer per epilogue warp");
+
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, uint32_t tmem, uint32_t col_base, int m0, int n0,
-                                              int q, int lane) {
-  const int row = m0 + 32 * q + lane;
+                                              int q, int lane, __nv_bfloat16* tb) {
+  const int rbase = m0 + 32 * q, row = rbase + lane;
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t r[32];
     tmem_ld32(tmem + (uint32_t(32 * q) << 16) + col_base + uint32_t(32 * c), r);
     const int col0 = n0 + 32 * c;
-    if (row >= g.M || col0 >= g.N) continue;
-    if (g.sym && col0 + 31 < row) continue;
+    if (rbase >= g.M || col0 >= g.N) continue;  // warp-uniform
+    const bool lane_ok = row < g.M && !(g.sym && col0 + 31 < row);
     __nv_bfloat16* drow = g.D + int64_t(row) * g.ldd;
-    const __nv_bfloat16* crow = g.C ? g.C + int64_t(row) * g.ldc : nullptr;
-    const bool cterm = crow && g.beta != 0.f;
+    const __nv_bfloat16* crow = (g.C && row < g.M) ? g.C + int64_t(row) * g.ldc : nullptr;
+    const bool cterm = lane_ok && crow && g.beta != 0.f;
     const bool cvec = cterm && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(crow + col0) & 15) == 0;
     __nv_bfloat162 o2[16];
 #pragma unroll
@@ -183,29 +190,46 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, uint32_t tmem, 
         o2[4 * v + j] = __floats2bfloat162_rn(lo, hi);
       }
     }
-    const bool whole = !g.sym || col0 >= row;
-    if (whole && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(drow + col0) & 15) == 0) {
+    if (lane_ok) {
+      const bool whole = !g.sym || col0 >= row;
+      if (whole && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(drow + col0) & 15) == 0) {
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint4 ow;
-        __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ow);
+        for (int v = 0; v < 4; ++v) {
+          uint4 ow;
+          __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ow);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) op[j] = o2[4 * v + j];
-        *reinterpret_cast<uint4*>(drow + col0 + 8 * v) = ow;
-      }
-    } else {
+          for (int j = 0; j < 4; ++j) op[j] = o2[4 * v + j];
+          *reinterpret_cast<uint4*>(drow + col0 + 8 * v) = ow;
+        }
+      } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int col = col0 + j;
-        if (col < g.N && (!g.sym || col >= row)) drow[col] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
+        for (int j = 0; j < 32; ++j) {
+          const int col = col0 + j;
+          if (col < g.N && (!g.sym || col >= row)) drow[col] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
+        }
       }
     }
-    if (g.sym) {
+    // mirror: D[col][row] for col > row, through the transposed block (the warp's
+    // block has such elements unless it lies wholly at or below the diagonal)
+    if (g.sym && col0 + 31 > rbase) {
+      __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int col = col0 + j;
-        if (col > row && col < g.N) g.D[int64_t(col) * g.ldd + row] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
+      for (int j = 0; j < 32; ++j) tb[j * kTbPitch + lane] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
+      __syncwarp();
+      const int mrow = col0 + lane;  // this lane's mirrored row: elements from rows rbase .. rbase + 31
+      if (mrow < g.N) {
+        __nv_bfloat16* dm = g.D + int64_t(mrow) * g.ldd + rbase;
+        const __nv_bfloat16* src = tb + lane * kTbPitch;
+        if (mrow > rbase + 31 && rbase + 31 < g.M && (reinterpret_cast<uintptr_t>(dm) & 15) == 0) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            reinterpret_cast<uint4*>(dm)[v] = reinterpret_cast<const uint4*>(src)[v];
+        } else {
+          for (int k = 0; k < 32; ++k)
+            if (rbase + k < mrow && rbase + k < g.M) dm[k] = src[k];
+        }
       }
+      __syncwarp();  // tb is rewritten by the next chunk
     }
   }
 }
@@ -352,6 +376,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue
     const int q = warp & 3;
+    auto* tb = reinterpret_cast<__nv_bfloat16*>(gbase + STAGES * STAGE_BYTES + 256 + (warp - 2) * kTbBytes);
     uint32_t tc = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       int m0, n0;
@@ -360,7 +385,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const bool ok = mbar_wait(tfull_bar(buf), (tc >> 1) & 1u, g.status, 4);
       tc_fence_after();
       if (!ok) break;
-      epilogue_tile(g, tmem, uint32_t(buf) * BN, m0, n0, q, lane);
+      epilogue_tile(g, tmem, uint32_t(buf) * BN, m0, n0, q, lane, tb);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(tempty_bar(buf));
