@@ -36,7 +36,7 @@ constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + 4 * 2560 /*mirror buffers*/;
+constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
 // X X^T and (A A^T with A symmetric) have symmetric results: compute the tiles
 // touching the upper triangle only and mirror them
@@ -125,9 +125,9 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits
 // 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B major in bit 16, N >> 3 in bits
 // 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn_major) << 16) | (uint32_t(n >> 3) << 17) |
-         (uint32_t(m >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int b_mn_major, int a_mn_major = 0) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
+         (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
 struct GemmArgs {
@@ -137,33 +137,34 @@ struct GemmArgs {
   __nv_bfloat16* D;        // output, row pitch ldd
   int64_t ldc, ldd;
   int* status;
-  int sym;     // D is symmetric (M == N): only tiles touching the upper triangle run, and mirror it
+  int sym;     // D is symmetric (M == N): only the tiles touching the upper triangle run (and are stored)
   int ntiles;  // tiles that run (symmetric: those touching the upper triangle), set by the launcher
+  int a_sym;   // the A operand is such a symmetric result: its tiles below the stored ones are read transposed
+  int b_sym;   // the same for a K-major B operand
 };
 
-// Epilogue of one 128 x 256 tile: TMEM accumulator columns [col_base, col_base +
-// 256) -> alpha * acc + beta * C -> bf16 D (symmetric results: columns >= row
-// written directly, those > row mirrored).  Called by the four epilogue warps;
-// q = the TMEM lane quarter the warp may access, lane = its row of the quarter.
-// The mirror goes through the warp's shared-memory buffer tb (32 rows of
-// kTbPitch bf16): the warp's 32 x 32 block is transposed there, so that each lane
-// writes one mirrored row of 32 elements with 16-byte stores.
-constexpr int kTbPitch = 40;  // bf16 per transposed row (80 bytes: 16-byte aligned rows)
-constexpr int kTbBytes = 32 * kTbPitch * 2;
-static_assert(kTbBytes == 2560, "the kernel reserves 2560 bytes of mirror buffer per epilogue warp");
+// A symmetric result is stored as the 128 x 256 output tiles that touch its
+// upper triangle, each written whole; the element (r, k) of a tile that was not
+// computed equals (k, r), which lies in a stored tile.  An operand box of 128
+// rows from r0 and 64 columns from k0 lies in one output tile: stored or not.
+__host__ __device__ __forceinline__ bool sym_stored(int r0, int k0) { return (k0 / BN) * BN + BN > r0; }
 
+// Epilogue of one 128 x 256 tile: TMEM accumulator columns [col_base, col_base +
+// 256) -> alpha * acc + beta * C -> bf16 D, the whole tile (symmetric results
+// too: their tiles touching the upper triangle are stored whole, nothing is
+// mirrored).  Called by the four epilogue warps; q = the TMEM lane quarter the
+// warp may access.
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, uint32_t tmem, uint32_t col_base, int m0, int n0,
-                                              int q, int lane, __nv_bfloat16* tb) {
-  const int rbase = m0 + 32 * q, row = rbase + lane;
+                                              int q, int lane) {
+  const int row = m0 + 32 * q + lane;
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t r[32];
     tmem_ld32(tmem + (uint32_t(32 * q) << 16) + col_base + uint32_t(32 * c), r);
     const int col0 = n0 + 32 * c;
-    if (rbase >= g.M || col0 >= g.N) continue;  // warp-uniform
-    const bool lane_ok = row < g.M && !(g.sym && col0 + 31 < row);
+    if (row >= g.M || col0 >= g.N) continue;
     __nv_bfloat16* drow = g.D + int64_t(row) * g.ldd;
-    const __nv_bfloat16* crow = (g.C && row < g.M) ? g.C + int64_t(row) * g.ldc : nullptr;
-    const bool cterm = lane_ok && crow && g.beta != 0.f;
+    const __nv_bfloat16* crow = g.C ? g.C + int64_t(row) * g.ldc : nullptr;
+    const bool cterm = crow && g.beta != 0.f;
     const bool cvec = cterm && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(crow + col0) & 15) == 0;
     __nv_bfloat162 o2[16];
 #pragma unroll
@@ -190,46 +191,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, uint32_t tmem, 
         o2[4 * v + j] = __floats2bfloat162_rn(lo, hi);
       }
     }
-    if (lane_ok) {
-      const bool whole = !g.sym || col0 >= row;
-      if (whole && col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(drow + col0) & 15) == 0) {
+    if (col0 + 32 <= g.N && (reinterpret_cast<uintptr_t>(drow + col0) & 15) == 0) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 ow;
-          __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ow);
+      for (int v = 0; v < 4; ++v) {
+        uint4 ow;
+        __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ow);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) op[j] = o2[4 * v + j];
-          *reinterpret_cast<uint4*>(drow + col0 + 8 * v) = ow;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = col0 + j;
-          if (col < g.N && (!g.sym || col >= row)) drow[col] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
-        }
+        for (int j = 0; j < 4; ++j) op[j] = o2[4 * v + j];
+        *reinterpret_cast<uint4*>(drow + col0 + 8 * v) = ow;
       }
-    }
-    // mirror: D[col][row] for col > row, through the transposed block (the warp's
-    // block has such elements unless it lies wholly at or below the diagonal)
-    if (g.sym && col0 + 31 > rbase) {
-      __syncwarp();
+    } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) tb[j * kTbPitch + lane] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
-      __syncwarp();
-      const int mrow = col0 + lane;  // this lane's mirrored row: elements from rows rbase .. rbase + 31
-      if (mrow < g.N) {
-        __nv_bfloat16* dm = g.D + int64_t(mrow) * g.ldd + rbase;
-        const __nv_bfloat16* src = tb + lane * kTbPitch;
-        if (mrow > rbase + 31 && rbase + 31 < g.M && (reinterpret_cast<uintptr_t>(dm) & 15) == 0) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            reinterpret_cast<uint4*>(dm)[v] = reinterpret_cast<const uint4*>(src)[v];
-        } else {
-          for (int k = 0; k < 32; ++k)
-            if (rbase + k < mrow && rbase + k < g.M) dm[k] = src[k];
-        }
-      }
-      __syncwarp();  // tb is rewritten by the next chunk
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < g.N) drow[col0 + j] = (j & 1) ? o2[j >> 1].y : o2[j >> 1].x;
     }
   }
 }
@@ -274,9 +248,15 @@ __device__ __forceinline__ void tile_at(int u, bool rows_first, int mt, int nt, 
   n0 = bn * BN;
 }
 
+// tmA / tmB: K-major boxes of 64 columns x BM / BN rows (B_MN: 64 x 64 boxes of
+// the K x N operand).  With a_sym / b_sym, tmAt / tmBt address the same matrices
+// in 64 x 64 boxes for the transposed (MN-major) reads of the k-blocks whose
+// tiles were not stored: a 128-row A box or 256-row B box of one k-block is
+// either stored whole or not at all.
 template <bool B_MN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    k_gemm_p(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+    k_gemm_p(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmBt, GemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -324,11 +304,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t a_dst = base + uint32_t(s) * STAGE_BYTES;
         const uint32_t b_dst = a_dst + A_STAGE;
         mbar_expect_tx(full_bar(s), STAGE_BYTES);
-        tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
+        if (g.a_sym && !sym_stored(m0, kb * BK)) {  // rows m0.. of the k-block, read as its transpose (MN-major)
+          tma_load_2d(a_dst, &tmAt, m0, kb * BK, full_bar(s));
+          tma_load_2d(a_dst + uint32_t(BK * 128), &tmAt, m0 + 64, kb * BK, full_bar(s));
+        } else {
+          tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
+        }
         if (B_MN) {
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
             tma_load_2d(b_dst + uint32_t(j) * (BK * 128), &tmB, n0 + 64 * j, kb * BK, full_bar(s));
+        } else if (g.b_sym && !sym_stored(n0, kb * BK)) {  // read transposed (MN-major), like B_MN
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(b_dst + uint32_t(j) * (BK * 128), &tmBt, n0 + 64 * j, kb * BK, full_bar(s));
         } else {
           tma_load_2d(b_dst, &tmB, kb * BK, n0, full_bar(s));
         }
@@ -339,7 +328,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_wait(full_bar(int(d % STAGES)), (d / STAGES) & 1u, g.status, 2);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(BM, BN, B_MN ? 1 : 0);
     uint32_t it = 0, tc = 0;  // k-blocks consumed, tiles done
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
@@ -358,12 +346,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_after();
         const uint32_t a_addr = base + uint32_t(s) * STAGE_BYTES;
         const uint32_t b_addr = a_addr + A_STAGE;
+        const bool a_t = g.a_sym && !sym_stored(m0, kb * BK);
+        const bool b_t = B_MN || (g.b_sym && !sym_stored(n0, kb * BK));
+        const uint32_t id = idesc_bf16(BM, BN, b_t ? 1 : 0, a_t ? 1 : 0);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = sdesc(a_addr + 32u * kk, 16, 1024);
-          const uint64_t bd = B_MN ? sdesc(b_addr + uint32_t(kk) * 16u * 128u, BK * 128, 1024)
-                                   : sdesc(b_addr + 32u * kk, 16, 1024);
-          mma_bf16(acc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          // K-major: 16-element k slices 32 bytes apart; MN-major: 16 k rows (2 KB)
+          // apart, 64-element M / N chunks one box (8 KB) apart
+          const uint64_t ad = a_t ? sdesc(a_addr + uint32_t(kk) * 16u * 128u, BK * 128, 1024)
+                                  : sdesc(a_addr + 32u * kk, 16, 1024);
+          const uint64_t bd = b_t ? sdesc(b_addr + uint32_t(kk) * 16u * 128u, BK * 128, 1024)
+                                  : sdesc(b_addr + 32u * kk, 16, 1024);
+          mma_bf16(acc, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
         }
         mma_commit(empty_bar(s));
       }
@@ -376,7 +370,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue
     const int q = warp & 3;
-    auto* tb = reinterpret_cast<__nv_bfloat16*>(gbase + STAGES * STAGE_BYTES + 256 + (warp - 2) * kTbBytes);
     uint32_t tc = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       int m0, n0;
@@ -385,7 +378,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const bool ok = mbar_wait(tfull_bar(buf), (tc >> 1) & 1u, g.status, 4);
       tc_fence_after();
       if (!ok) break;
-      epilogue_tile(g, tmem, uint32_t(buf) * BN, m0, n0, q, lane, tb);
+      epilogue_tile(g, tmem, uint32_t(buf) * BN, m0, n0, q, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(tempty_bar(buf));
@@ -606,7 +599,8 @@ int check_mat(const bq_mat& t) {
   return BQ_OK;
 }
 
-int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, cudaStream_t s) {
+int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tat, const CUtensorMap& tbt,
+         const GemmArgs& g, cudaStream_t s) {
   if (once_per_device(kOnceGemmAttr)) {  // the attribute belongs to the current device
     if (cudaFuncSetAttribute(k_gemm_p<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(k_gemm_p<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) != cudaSuccess)
@@ -622,9 +616,9 @@ int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs
   if (a.ntiles == 0) return BQ_OK;
   const unsigned grid = unsigned(std::min(a.ntiles, sm_count()));
   if (b_mn)
-    k_gemm_p<true><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, a);
+    k_gemm_p<true><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, tat, tbt, a);
   else
-    k_gemm_p<false><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, a);
+    k_gemm_p<false><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, tat, tbt, a);
   return check("bq_muon_ns (gemm)");
 }
 
@@ -663,7 +657,7 @@ int ns_one(const bq_mat& t, unsigned char* w, int* status, int steps, float a, f
   if (int rc = check("bq_muon_ns (scale)")) return rc;
 
   // tensor maps: X as K-major A operand / K-major B operand / MN-major B operand, A, B
-  CUtensorMap mXa[2], mXb[2], mXmn[2], mAa, mAb, mBa;
+  CUtensorMap mXa[2], mXb[2], mXmn[2], mAa, mAb, mAmn, mBa, mBmn;
   __nv_bfloat16* Xs[2] = {X0, X1};
   for (int j = 0; j < 2; ++j) {
     if (int rc = make_map(&mXa[j], Xs[j], p.n, p.m, p.ldx, BM)) return rc;
@@ -672,20 +666,22 @@ int ns_one(const bq_mat& t, unsigned char* w, int* status, int steps, float a, f
   }
   if (int rc = make_map(&mAa, A, p.m, p.m, p.lda, BM)) return rc;
   if (int rc = make_map(&mAb, A, p.m, p.m, p.lda, BN)) return rc;
+  if (int rc = make_map(&mAmn, A, p.m, p.m, p.lda, BK)) return rc;  // 64 x 64 boxes: transposed reads
   if (int rc = make_map(&mBa, B, p.m, p.m, p.lda, BM)) return rc;
+  if (int rc = make_map(&mBmn, B, p.m, p.m, p.lda, BK)) return rc;
 
   int cur = 0;
   for (int it = 0; it < steps; ++it) {
     const int nxt = cur ^ 1;
-    // A = X X^T
-    GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status, kSymmetric, 0};
-    if (int rc = gemm(false, mXa[cur], mXb[cur], g1, s)) return rc;
-    // B = c (A A^T) + b A   (A symmetric)
-    GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric, 0};
-    if (int rc = gemm(false, mAa, mAb, g2, s)) return rc;
-    // X' = B X + a X
-    GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0, 0};
-    if (int rc = gemm(true, mBa, mXmn[cur], g3, s)) return rc;
+    // A = X X^T (symmetric: the tiles touching the upper triangle)
+    GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status, kSymmetric, 0, 0, 0};
+    if (int rc = gemm(false, mXa[cur], mXb[cur], mXa[cur], mXa[cur], g1, s)) return rc;
+    // B = c (A A^T) + b A   (A symmetric and stored as such: both operands read it)
+    GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric, 0, kSymmetric, kSymmetric};
+    if (int rc = gemm(false, mAa, mAb, mAmn, mAmn, g2, s)) return rc;
+    // X' = B X + a X   (B symmetric and stored as such)
+    GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0, 0, kSymmetric, 0};
+    if (int rc = gemm(true, mBa, mXmn[cur], mBmn, mBmn, g3, s)) return rc;
     cur = nxt;
   }
   // y = X (transposed back for a tall input)
