@@ -9,9 +9,11 @@
 // shared memory, tcgen05.mma issued by one thread into one of two TMEM fp32
 // accumulators, an epilogue reading TMEM with tcgen05.ld and writing
 // D = alpha*acc + beta*C in bf16 while the next tile's products run.  A is
-// symmetric, so A A is computed as A A^T (both operands K-major), and the two
-// symmetric products run only the tiles touching the upper triangle and mirror
-// them; B X takes X as an MN-major operand.
+// symmetric, so A A is computed as A A^T (both operands K-major).  The two
+// symmetric products run and store only the tiles touching the upper triangle;
+// a product reading A or B takes each k-block lying below those tiles as the
+// transpose of its stored partner (MN-major TMA boxes and descriptors), so no
+// lower half is ever written.  B X takes X as an MN-major operand.
 //
 // Every wait on an mbarrier is bounded: on timeout the kernel records an error
 // word in the workspace, drains its own copies, frees TMEM and returns.
@@ -38,8 +40,8 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
-// X X^T and (A A^T with A symmetric) have symmetric results: compute the tiles
-// touching the upper triangle only and mirror them
+// X X^T and (A A^T with A symmetric) have symmetric results: compute and store the
+// tiles touching the upper triangle only (0: every product runs whole)
 #ifndef BQ_NS_SYMMETRIC
 #define BQ_NS_SYMMETRIC 1
 #endif
