@@ -162,7 +162,7 @@ def muon_flops(shapes, steps=5):
 def muon_executed_flops(shapes, steps=5, bm=128, bn=256):
     """FLOPs the tensor cores execute per batch: whole 128 x 256 tiles, and for the
     two symmetric products (X X^T, A A^T) only the tiles that touch the upper
-    triangle (the kernel mirrors them)."""
+    triangle (the only ones the kernel computes and stores)."""
     tot = 0
     for r, c in shapes:
         m, n = min(r, c), max(r, c)
@@ -896,7 +896,7 @@ def run_ours(args):
             line["muon"] = {"value": round(tf, 1), "unit": "TFLOP/s", "ms": round(muon_ms_max, 3),
                             "flops": muon.flops,
                             "count": "nominal 4 m^2 n + 2 m^3 per step; X X^T and A A^T are computed on "
-                                     "the upper triangle and mirrored, so this is an effective rate",
+                                     "the tiles touching the upper triangle only, so this is an effective rate",
                             "executed_flops": ex, "executed_TFLOP/s": round(ex_tf, 1),
                             "frac": round(ex_tf / world / pk["bf16"], 4),
                             "frac_basis": "executed FLOPs (the tiles that run) / measured burst bf16 peak",
