@@ -574,6 +574,16 @@ __device__ __forceinline__ bool block_staged(int64_t start, int nel) { return ne
 // barrier of the consumer warps only (the producer never joins it)
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(32 * kCons) : "memory"); }
 
+// A consumer warp hands a ring stage back after reading it.  The reads went
+// through the generic proxy and the producer's next bulk copy into the stage
+// writes through the async proxy, which the mbarrier alone does not order: each
+// lane fences between the two proxies before the warp arrives.
+__device__ __forceinline__ void release_stage(uint64_t* empty, int lane) {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty);
+}
+
 __device__ __forceinline__ void strip_producer(const RegionGroup* __restrict__ groups, int ngroups, const AdamArgs& a,
                                                TmaStage* ring, uint64_t* full, uint64_t* empty, int lane) {
   uint32_t k = 0;  // stages issued
@@ -709,8 +719,7 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
         x = raw_from_global(a, pos, n);
       }
       const float sm = S.sc[2 * warp], sv = S.sc[2 * warp + 1];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // this warp no longer reads the stage
+      release_stage(&empty[s], lane);  // this warp no longer reads the stage
       Lane8 o;
       if (staged) adam_raw<true>(h, x, 8, sm, sv, o);
       else adam_raw<false>(h, x, n, sm, sv, o);

@@ -153,6 +153,19 @@ def test_dequant_view_bit_exact(cuda, name, dev):
     assert_bits_equal("bf16 view", out.cpu().numpy().view(np.uint16), want)
 
 
+def test_very_wide_band(cuda):
+    """A 2-row band of 524,408 columns (4097 FP8 column tiles, the last 120 wide)
+    beside a ragged 130-row band: every Adam piece of the wide band lies inside one
+    row pair and its FP8 tiles are single groups of the two-pass quantiser."""
+    c = W.config("toy")
+    c.cfg_id = 43
+    T = W.TensorSpec
+    tensors = [T("wide_band", 2, 4097 * 128 - 8, 128 * (4097 * 128 - 8), W.ADAM_FLAT256, True),
+               T("band_2d", 130, 360, 128 * 360, W.ADAM_FLAT256, True)]
+    case = StepCase(c, tensors=tensors, V=1, dev_lo=0, dev_hi=1)
+    _compare(case, case.run_gpu(cuda), case.run_oracle())
+
+
 @pytest.mark.parametrize("name", ["gptoss-small", "odd-start"])
 def test_start_align_8(cuda, name):
     """Planned with 8-element starts: regions may begin 8 elements off a 16-element
