@@ -680,7 +680,6 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
   bool dead = false;   // a wait timed out: skip the remaining work, keep the barriers
   for (int gi = ngroups - 1 - int(blockIdx.x); gi >= 0; gi -= int(gridDim.x)) {
     const RegionGroup g = groups[gi];
-    const bool flat = g.width == g.C;
     const bool fp8 = FP8 && g.fslot >= 0;  // band pieces carry no FP8 (their tiles are quantised apart)
     const int ntile = (g.width + 127) >> 7;
     const int nel = g.rows * g.width;
