@@ -826,6 +826,27 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
 constexpr int kTileTmemCols = 128;
 static_assert(kAdamCtas * kTileTmemCols <= 512, "the resident CTAs' TMEM columns fit one SM");
 
+// L2 prefetch of rows [r0, r0 + 32) of tile g: a row is 8 lines (master 4,
+// gradient 2, m 1, v 1), one per thread.  Issued one load round ahead, it lets the
+// next round's loads hit L2 without holding registers (prefetching a whole tile
+// ahead instead thrashed L2: slower)
+__device__ __forceinline__ void tile_prefetch(const RegionGroup& g, int r0, const AdamArgs& a) {
+  const int r = r0 + (int(threadIdx.x) >> 3), kind = int(threadIdx.x) & 7;
+  if (r >= g.rows) return;
+  const int64_t row = g.pos + int64_t(r) * g.C;
+  const void* p;
+  if (kind < 4) {
+    if (32 * kind >= g.width) return;
+    p = a.master + row + 32 * kind;
+  } else if (kind < 6) {
+    if (64 * (kind - 4) >= g.width) return;
+    p = a.grad + row + 64 * (kind - 4);
+  } else {
+    p = kind == 6 ? static_cast<const void*>(a.m + row) : static_cast<const void*>(a.v + row);
+  }
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
 __device__ __forceinline__ void block_max(uint32_t x, uint32_t* red, int which) {
   x = __reduce_max_sync(0xFFFFFFFFu, x);
   if ((threadIdx.x & 31) == 0) red[which * kWarps + (threadIdx.x >> 5)] = x;
@@ -889,6 +910,9 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
       }
       const Raw8 x0 = raw_from_global(a, pos0, ok0 ? 8 : 0);
       const Raw8 x1 = raw_from_global(a, pos1, ok1 ? 8 : 0);
+      // the next 32 rows (or the next tile's first 32) into L2 while these are used
+      if (i < 6) tile_prefetch(g, 16 * (i + 2), a);
+      else if (gi >= int(gridDim.x)) tile_prefetch(groups[gi - int(gridDim.x)], 0, a);
       uint32_t w[8];
       pack_inputs(x0, w);
       __syncwarp();
@@ -1011,6 +1035,20 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGrou
       const int64_t p0 = ok0 ? vpos(v0) : g.pos, p1 = ok1 ? vpos(v1) : g.pos;
       const Raw8 x0 = raw_from_global(a, p0, ok0 ? 8 : 0);
       const Raw8 x1 = raw_from_global(a, p1, ok1 ? 8 : 0);
+      {  // this warp's next 16 rows (or the next group's first 16) into L2: lane -> row, two lines each
+        const RegionGroup* ng = i == 0 ? &g : (gi >= int(gridDim.x) ? &groups[gi - int(gridDim.x)] : nullptr);
+        const int r = (i == 0 ? 16 : 0) + (lane & 15);
+        if (ng && c < ng->width && r < ng->rows) {
+          const int64_t row = ng->pos + int64_t(r) * ng->C + c;
+          if (lane < 16) {
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.master + row));
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.grad + row));
+          } else {
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.m + row));
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.v + row));
+          }
+        }
+      }
       uint32_t w[8];
       pack_inputs(x0, w);
       __syncwarp();  // tcgen05 loads and stores are issued by the whole warp
