@@ -870,6 +870,9 @@ def run_ours(args):
             "config": workload_config(head["describe"], head["bytes"], head["S"], head["n"], head["members"],
                                       bool(muon), world),
             "hbm_frac": round(value / world / pk["hbm"], 4),
+            "useful": {"GB/s": round(job_throughput(B - 2 * head["bytes"]["pads"], world, dbuf_ms_max) / 1e9, 1),
+                       "bytes": B - 2 * head["bytes"]["pads"],
+                       "note": "value without the pack's 2 B zero write per padding element"},
             "dbuffer_ms": round(dbuf_ms_max, 4),
             "pack": {"ms": round(statistics.mean(pack_ms), 4),
                      "GB/s": round(gbs(head["bytes"]["pack"], statistics.mean(pack_ms)), 1),
