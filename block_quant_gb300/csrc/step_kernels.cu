@@ -826,6 +826,12 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
 constexpr int kTileTmemCols = 128;
 static_assert(kAdamCtas * kTileTmemCols <= 512, "the resident CTAs' TMEM columns fit one SM");
 
+// row of vector v of a region with vpr vectors a row: full tile rows (vpr 16 or
+// 4, a power of two, warp-uniform) take a shift instead of an integer division
+__device__ __forceinline__ int vec_row(int v, int vpr) {
+  return (vpr & (vpr - 1)) == 0 ? v >> (__ffs(vpr) - 1) : v / vpr;
+}
+
 // L2 prefetch of rows [r0, r0 + 32) of tile g: a row is 8 lines (master 4,
 // gradient 2, m 1, v 1), one per thread.  Issued one load round ahead, it lets the
 // next round's loads hit L2 without holding registers (prefetching a whole tile
@@ -901,11 +907,11 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
     for (int i = 0; i < 8 && kThreads * i + 32 * warp < nvec; i += 2) {
       const int v0 = threadIdx.x + kThreads * i, v1 = v0 + kThreads;
       const bool ok0 = v0 < nvec, ok1 = v1 < nvec;
-      const int r0 = v0 / vpr, k0 = v0 - r0 * vpr;
+      const int r0 = vec_row(v0, vpr), k0 = v0 - r0 * vpr;
       const int64_t pos0 = g.pos + int64_t(r0) * g.C + (k0 << 3);
       int64_t pos1 = pos0;
       if (ok1) {
-        const int r1 = v1 / vpr, k1 = v1 - r1 * vpr;
+        const int r1 = vec_row(v1, vpr), k1 = v1 - r1 * vpr;
         pos1 = g.pos + int64_t(r1) * g.C + (k1 << 3);
       }
       const Raw8 x0 = raw_from_global(a, pos0, ok0 ? 8 : 0);
@@ -964,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
       tmem_ld8(tcell + uint32_t(8 * i), w);
       const int v = threadIdx.x + kThreads * i;
       if (v < nvec) {
-        const int r = v / vpr, k = v - r * vpr;
+        const int r = vec_row(v, vpr), k = v - r * vpr;
         const int64_t pos = g.pos + int64_t(r) * g.C + (k << 3);
         Raw8 x;
         unpack_inputs(w, x);
@@ -1025,7 +1031,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile32(const RegionGrou
     const int slot = g.mslot + warp;
     const float sm = a.m_scale[slot], sv = a.v_scale[slot];
     auto vpos = [&](int v) {
-      const int r = v / vpr, k = v - r * vpr;
+      const int r = vec_row(v, vpr), k = v - r * vpr;
       return g.pos + int64_t(r) * g.C + c + (k << 3);
     };
     uint32_t am = 0, av = 0;
@@ -1242,7 +1248,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_region(const RegionGroup* __
           col = (v << 3) % g.C;
           pos = g.pos + (int64_t(v) << 3);
         } else {
-          const int r = v / vpr, k = v - r * vpr;
+          const int r = vec_row(v, vpr), k = v - r * vpr;
           col = k << 3;
           pos = g.pos + int64_t(r) * g.C + col;
         }
@@ -1334,7 +1340,7 @@ __global__ void __launch_bounds__(kThreads) k_dequant_region(const RegionGroup* 
         col = int(e - fastdiv(e, g.cmul, g.cshr) * uint32_t(g.C));
         pos = g.pos + e;
       } else {
-        const int r = v / vpr, k = v - r * vpr;
+        const int r = vec_row(v, vpr), k = v - r * vpr;
         col = k << 3;
         pos = g.pos + int64_t(r) * g.C + col;
       }
