@@ -885,8 +885,9 @@ template <bool FP8>
 __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup* __restrict__ groups, int ngroups, AdamArgs a) {
   __shared__ uint32_t red[3 * kWarps];
   __shared__ uint32_t s_tmem;
-  // FP8: the tile's p', thread t's vector i at float4 pair 2 (256 i + t): the
-  // second phase converts it from here instead of re-reading the master
+  // FP8: the tile's p', vector v (= 256 i + t) as float4s v and 2048 + v (a warp's
+  // 16-byte accesses are contiguous, free of bank conflicts): the second phase
+  // converts it from here instead of re-reading the master
   extern __shared__ float4 s_p[];
   const int warp = threadIdx.x >> 5;
   if (warp == 0) tmem_alloc(smem_u32(&s_tmem), kTileTmemCols);
@@ -931,7 +932,11 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
       if (ok0) {
         adam_raw<true>(h, x0, 8, sm, sv, o);
         store_p8(a.master + pos0, o.p1);
-        if (fp8) store_p8(reinterpret_cast<float*>(s_p + 2 * (kThreads * i + int(threadIdx.x))), o.p1);
+        if (fp8) {
+          const int vi = kThreads * i + int(threadIdx.x);
+          s_p[vi] = make_float4(o.p1[0], o.p1[1], o.p1[2], o.p1[3]);
+          s_p[8 * kThreads + vi] = make_float4(o.p1[4], o.p1[5], o.p1[6], o.p1[7]);
+        }
         am = max(am, o.am);
         av = max(av, o.av);
         ap = max(ap, o.ap);
@@ -939,7 +944,11 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
       if (ok1) {
         adam_raw<true>(h, x1, 8, sm, sv, o);
         store_p8(a.master + pos1, o.p1);
-        if (fp8) store_p8(reinterpret_cast<float*>(s_p + 2 * (kThreads * (i + 1) + int(threadIdx.x))), o.p1);
+        if (fp8) {
+          const int vi = kThreads * (i + 1) + int(threadIdx.x);
+          s_p[vi] = make_float4(o.p1[0], o.p1[1], o.p1[2], o.p1[3]);
+          s_p[8 * kThreads + vi] = make_float4(o.p1[4], o.p1[5], o.p1[6], o.p1[7]);
+        }
         am = max(am, o.am);
         av = max(av, o.av);
         ap = max(ap, o.ap);
@@ -980,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
         *reinterpret_cast<uint2*>(a.m + pos) = codes_int8(o.m1, qm);
         *reinterpret_cast<uint2*>(a.v + pos) = codes_uint8(o.v1, qv);
         if (fp8) {  // this thread's p' of vector v, kept in shared memory by the first phase
-          const float4 p0 = s_p[2 * v], p1 = s_p[2 * v + 1];
+          const float4 p0 = s_p[v], p1 = s_p[8 * kThreads + v];
           const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
           *reinterpret_cast<uint2*>(a.fp8 + pos) = codes_e4m3(pv, qp);
         }
