@@ -817,6 +817,8 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
 // Phase 1: Adam, write master, block-reduce max|m'|, max v', max|p'|; each
 // element's inputs (bf16 gradient, m code, v code) also go to tensor memory as
 // one packed 32-bit word, and with FP8 its p' to shared memory (64 KB a tile).
+// Its loads go in four rounds of two vectors a thread; each round first asks L2
+// for the next round's lines (the last one for the next tile's first rows).
 // Phase 2: requantise m', v' (recomputed bit-identically from those words and
 // the old scales held in registers) and convert p' from shared memory.
 // Thread t handles the tile's vectors t + 256 i (i < 8, a tile has at most 2048
