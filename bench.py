@@ -700,6 +700,23 @@ def cpu_baseline(workload=WORKLOAD, single_seconds=8.0):
             **info}
 
 
+def cpu_baseline_muon(n=4096, steps=5, seed=5):
+    """The oracle's Newton-Schulz (fp64 numpy, the BLAS library's own threads over
+    the host cores) on a bounded sample of the batch: its n x n matrix, `steps`
+    iterations, seeded N(0, 1e-3) entries.  TFLOP/s on the nominal count."""
+    from oracle import muon as OM
+
+    x = np.random.default_rng(seed).standard_normal((n, n)) * 1e-3
+    t0 = time.perf_counter()
+    OM.newton_schulz(x, steps=steps)
+    dt = time.perf_counter() - t0
+    flops = steps * OM.ns_cost(n, n)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    return {"value": round(flops / dt / 1e12, 4), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"the batch's {n}x{n} matrix, {steps} Newton-Schulz steps in fp64 numpy (BLAS threads over "
+                      f"the host cores), {dt:.1f} s; nominal 4 m^2 n + 2 m^3 per step"}
+
+
 def time_group(step, stream, steps, warmup):
     """Mean pack and Adam milliseconds of a GroupStep (CUDA events)."""
     import torch
@@ -969,6 +986,8 @@ def run_ours(args):
                 "note": "measured after the timed region; not part of value"}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.workload)
+            if muon:
+                line["cpu_baseline"]["muon"] = cpu_baseline_muon()
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
