@@ -37,7 +37,8 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int EPI_WARPS = 8;       // two per TMEM lane quarter, each half of a tile's columns
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA + TMEM, then the epilogue
 constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
 // X X^T and (A A^T with A symmetric) have symmetric results: compute and store the
@@ -154,12 +155,12 @@ __host__ __device__ __forceinline__ bool sym_stored(int r0, int k0) { return (k0
 // Epilogue of one 128 x 256 tile: TMEM accumulator columns [col_base, col_base +
 // 256) -> alpha * acc + beta * C -> bf16 D, the whole tile (symmetric results
 // too: their tiles touching the upper triangle are stored whole, nothing is
-// mirrored).  Called by the four epilogue warps; q = the TMEM lane quarter the
-// warp may access.
+// mirrored).  Called by the eight epilogue warps, two per TMEM lane quarter q (the
+// quarter the warp may access), each for the 32-column chunks [c_lo, c_hi).
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, uint32_t tmem, uint32_t col_base, int m0, int n0,
-                                              int q, int lane) {
+                                              int q, int lane, int c_lo, int c_hi) {
   const int row = m0 + 32 * q + lane;
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = c_lo; c < c_hi; ++c) {
     uint32_t r[32];
     tmem_ld32(tmem + (uint32_t(32 * q) << 16) + col_base + uint32_t(32 * c), r);
     const int col0 = n0 + 32 * c;
@@ -219,7 +220,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, uint32_t tmem, 
 // skip the tiles wholly below the diagonal).  The stage ring runs on across
 // tiles, and two TMEM accumulators alternate so that the epilogue of one tile
 // overlaps the main loop of the next: the MMA warp waits for an accumulator's
-// "empty" barrier (the four epilogue warps' arrivals) before reusing it, and
+// "empty" barrier (the eight epilogue warps' arrivals) before reusing it, and
 // commits its "full" barrier when the tile's products are done.
 constexpr int TMEM_COLS_P = 2 * BN;
 
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);   // the MMA warp's commit
-      mbar_init(tempty_bar(b), 4);  // one arrival per epilogue warp
+      mbar_init(tempty_bar(b), EPI_WARPS);  // one arrival per epilogue warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -380,7 +381,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const bool ok = mbar_wait(tfull_bar(buf), (tc >> 1) & 1u, g.status, 4);
       tc_fence_after();
       if (!ok) break;
-      epilogue_tile(g, tmem, uint32_t(buf) * BN, m0, n0, q, lane);
+      const int half = (warp - 2) >> 2;  // warps 2-5: columns 0-127, warps 6-9: 128-255
+      epilogue_tile(g, tmem, uint32_t(buf) * BN, m0, n0, q, lane, half * (BN / 64), (half + 1) * (BN / 64));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(tempty_bar(buf));
