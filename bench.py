@@ -764,10 +764,10 @@ def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)  # before the process group, so NCCL binds each rank to its own GPU
     if world > 1:
         dist.init_process_group("nccl")
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
     import block_quant_gb300 as bq
 
     bq.load()
