@@ -962,14 +962,23 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
     __syncwarp();
     tmem_wait_st();
     __syncthreads();
-    uint32_t tm = 0, tv = 0, tp = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      tm = max(tm, red[w]);
-      tv = max(tv, red[kWarps + w]);
-      tp = max(tp, red[2 * kWarps + w]);
-    }
-    const QScale qm = qscale(tm, 127.f), qv = qscale(tv, 255.f), qp = qscale(tp, 448.f);
+    // each warp combines the 3 x kWarps maxima with one word a lane; lanes 0, 1
+    // and 2 derive the m, v and p' scales side by side and the warp shares them
+    static_assert(3 * kWarps <= 32, "one maximum word per lane");
+    const int lane = threadIdx.x & 31;
+    const uint32_t word = lane < 3 * kWarps ? red[lane] : 0u;
+    const uint32_t tm = __reduce_max_sync(0xFFFFFFFFu, lane < kWarps ? word : 0u);
+    const uint32_t tv = __reduce_max_sync(0xFFFFFFFFu, lane >= kWarps && lane < 2 * kWarps ? word : 0u);
+    const uint32_t tp = __reduce_max_sync(0xFFFFFFFFu, lane >= 2 * kWarps ? word : 0u);
+    const QScale q3 = qscale(lane == 0 ? tm : lane == 1 ? tv : tp, lane == 0 ? 127.f : lane == 1 ? 255.f : 448.f);
+    auto take = [&](int from) {
+      QScale q;
+      q.s = __shfl_sync(0xFFFFFFFFu, q3.s, from);
+      q.r = __shfl_sync(0xFFFFFFFFu, q3.r, from);
+      q.mode = __shfl_sync(0xFFFFFFFFu, q3.mode, from);
+      return q;
+    };
+    const QScale qm = take(0), qv = take(1), qp = take(2);
     if (threadIdx.x == 0) {
       a.m_scale[g.mslot] = qm.s;
       a.v_scale[g.mslot] = qv.s;
