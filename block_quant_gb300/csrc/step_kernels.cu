@@ -815,11 +815,12 @@ __global__ void __launch_bounds__(kStripThreads, kStripCtas) k_strip(const Regio
 
 // ---------------------------------------------------------------- 128x128 Adam tiles (+ FP8 of the same tile)
 // Phase 1: Adam, write master, block-reduce max|m'|, max v', max|p'|; each
-// element's inputs (bf16 gradient, m code, v code) also go to tensor memory as
-// one packed 32-bit word, and with FP8 its p' to shared memory (64 KB a tile).
+// vector's inputs (bf16 gradients, m codes, v codes: 32 bits an element) also
+// go to tensor memory as loaded, and with FP8 its p' to shared memory (64 KB a
+// tile).
 // Its loads go in four rounds of two vectors a thread; each round first asks L2
 // for the next round's lines (the last one for the next tile's first rows).
-// Phase 2: requantise m', v' (recomputed bit-identically from those words and
+// Phase 2: requantise m', v' (recomputed bit-identically from those inputs and
 // the old scales held in registers) and convert p' from shared memory.
 // Thread t handles the tile's vectors t + 256 i (i < 8, a tile has at most 2048
 // eight-element vectors); vector i's words live in the thread's TMEM lane (lane
@@ -860,27 +861,24 @@ __device__ __forceinline__ void block_max(uint32_t x, uint32_t* red, int which) 
   if ((threadIdx.x & 31) == 0) red[which * kWarps + (threadIdx.x >> 5)] = x;
 }
 
-// element e's word: bf16 gradient bits << 16 | m code << 8 | v code
+// A vector's inputs as they were loaded, in 8 tensor-memory words: the four
+// words of bf16 gradient pairs, the two of m codes, the two of v codes (the
+// same 32 bits an element as any packed form, with no repacking either way)
 __device__ __forceinline__ void pack_inputs(const Raw8& x, uint32_t* w) {
-  const uint32_t gw[4] = {x.g.x, x.g.y, x.g.z, x.g.w};
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {  // elements 4h .. 4h + 3
-    const uint32_t mw = h ? x.m.y : x.m.x, vw = h ? x.v.y : x.v.x;
-    const uint32_t mv01 = __byte_perm(vw, mw, 0x5140u), mv23 = __byte_perm(vw, mw, 0x7362u);  // v0 m0 v1 m1, v2 m2 v3 m3
-    w[4 * h + 0] = __byte_perm(mv01, gw[2 * h], 0x5410u);
-    w[4 * h + 1] = __byte_perm(mv01, gw[2 * h], 0x7632u);
-    w[4 * h + 2] = __byte_perm(mv23, gw[2 * h + 1], 0x5410u);
-    w[4 * h + 3] = __byte_perm(mv23, gw[2 * h + 1], 0x7632u);
-  }
+  w[0] = x.g.x;
+  w[1] = x.g.y;
+  w[2] = x.g.z;
+  w[3] = x.g.w;
+  w[4] = x.m.x;
+  w[5] = x.m.y;
+  w[6] = x.v.x;
+  w[7] = x.v.y;
 }
 
 __device__ __forceinline__ void unpack_inputs(const uint32_t* w, Raw8& x) {
-  x.g = make_uint4(__byte_perm(w[0], w[1], 0x7632u), __byte_perm(w[2], w[3], 0x7632u), __byte_perm(w[4], w[5], 0x7632u),
-                   __byte_perm(w[6], w[7], 0x7632u));
-  x.m = make_uint2(__byte_perm(__byte_perm(w[0], w[1], 0x0051u), __byte_perm(w[2], w[3], 0x0051u), 0x5410u),
-                   __byte_perm(__byte_perm(w[4], w[5], 0x0051u), __byte_perm(w[6], w[7], 0x0051u), 0x5410u));
-  x.v = make_uint2(__byte_perm(__byte_perm(w[0], w[1], 0x0040u), __byte_perm(w[2], w[3], 0x0040u), 0x5410u),
-                   __byte_perm(__byte_perm(w[4], w[5], 0x0040u), __byte_perm(w[6], w[7], 0x0040u), 0x5410u));
+  x.g = make_uint4(w[0], w[1], w[2], w[3]);
+  x.m = make_uint2(w[4], w[5]);
+  x.v = make_uint2(w[6], w[7]);
 }
 
 template <bool FP8>
@@ -1021,9 +1019,9 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_tile(const RegionGroup*
 // 6.3): 32x32 blocks of the 2-D view, kept whole on one device by a 32-row
 // granularity.  A group is a 32-row band x <= 256 columns; warp w takes the
 // group's tile w (1..4 eight-element vectors per row).  Phase 1: Adam over the
-// tile, p' written, max|m'| and max v' reduced over the warp; each element's
-// inputs (bf16 gradient, m code, v code) also go to tensor memory as one packed
-// word.  Phase 2: m' and v' recomputed bit-identically from those words and
+// tile, p' written, max|m'| and max v' reduced over the warp; each vector's
+// inputs (bf16 gradients, m and v codes) also go to tensor memory as loaded.
+// Phase 2: m' and v' recomputed bit-identically from those words and
 // requantised.  Lane l handles the tile's vectors l + 32 i (i < 4); vector i's
 // words live in the lane's TMEM row (lane quarter warp % 4) at columns
 // 32 (warp / 4) + 8 i .. + 7: 64 columns per CTA.
