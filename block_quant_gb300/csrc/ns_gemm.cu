@@ -4,16 +4,17 @@
 // iteration (feynmanwiki walkthrough of veScale-FSDP, paper section 6.3).  Per
 // matrix (a tall one is iterated as its transpose):
 //   X = x / (||x||_F + eps);  repeat: A = X X^T;  B = b A + c A A;  X = a X + B X
-// Every product runs in k_gemm_p, a persistent kernel (one CTA per SM walking the
-// 128 x 256 output tiles): bf16 operands staged by TMA into 128-byte swizzled
-// shared memory, tcgen05.mma issued by one thread into one of two TMEM fp32
-// accumulators, an epilogue reading TMEM with tcgen05.ld and writing
-// D = alpha*acc + beta*C in bf16 while the next tile's products run.  A is
-// symmetric, so A A is computed as A A^T (both operands K-major).  The two
-// symmetric products run and store only the tiles touching the upper triangle;
-// a product reading A or B takes each k-block lying below those tiles as the
-// transpose of its stored partner (MN-major TMA boxes and descriptors), so no
-// lower half is ever written.  B X takes X as an MN-major operand.
+// The products run in persistent kernels: bf16 operands staged by TMA into
+// 128-byte swizzled shared memory, tcgen05.mma issued by one thread into one of
+// two TMEM fp32 accumulators, an epilogue reading TMEM with tcgen05.ld and
+// writing D = alpha*acc + beta*C in bf16 while the next tile's products run.
+// k_gemm_p (one CTA per SM, 128 x 256 tiles) runs the two symmetric products;
+// A is symmetric, so A A is computed as A A^T (both operands K-major).  They run
+// and store only the tiles touching the upper triangle; a product reading A or B
+// takes each k-block lying below those tiles as the transpose of its stored
+// partner (MN-major TMA boxes and descriptors), so no lower half is ever
+// written.  k_gemm_2 runs B X on pairs of CTAs (cta_group::2, 256 x 256 tiles,
+// M = 256 products reading both CTAs' shared memory), X an MN-major operand.
 //
 // Every wait on an mbarrier is bounded: on timeout the kernel records an error
 // word in the workspace, drains its own copies, frees TMEM and returns.
@@ -211,13 +212,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, uint32_t tmem, 
   }
 }
 
-// D[M x N] = alpha * (A[M x K] . op(B)) + beta * C.  A: K-major tensor map
-// (box 64 x 128).  B_MN = false: B given as [N x K] K-major (box 64 x 256), the
-// product is A B^T.  B_MN = true: B given as [K x N] N-contiguous (box 64 x 64,
-// four boxes per stage), the product is A B.
-// One CTA per SM walks the tiles t = blockIdx.x, + gridDim.x, ...
-// (B X: row blocks fastest; the others: column blocks fastest; symmetric results
-// skip the tiles wholly below the diagonal).  The stage ring runs on across
+// D[M x N] = alpha * (A[M x K] . B^T) + beta * C, A and B K-major: the two
+// products with symmetric results, X X^T and A A^T (B X runs on CTA pairs, below).
+// One CTA per SM walks the tiles t = blockIdx.x, + gridDim.x, ... (column blocks
+// fastest; symmetric results skip the tiles wholly below the diagonal).  The
+// stage ring runs on across
 // tiles, and two TMEM accumulators alternate so that the epilogue of one tile
 // overlaps the main loop of the next: the MMA warp waits for an accumulator's
 // "empty" barrier (the eight epilogue warps' arrivals) before reusing it, and
@@ -228,11 +227,11 @@ __device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// u-th tile that runs -> (m0, n0).  Full products: every tile, row blocks fastest
-// (B X) or column blocks fastest.  Symmetric results: the tiles touching the upper
-// triangle, listed row block by row block (row block bm starts at column block
-// floor(bm BM / BN)), so the CTAs share out only tiles with work.
-__device__ __forceinline__ void tile_at(int u, bool rows_first, int mt, int nt, int sym, int& m0, int& n0) {
+// u-th tile that runs -> (m0, n0).  Full products: every tile, column blocks
+// fastest.  Symmetric results: the tiles touching the upper triangle, listed row
+// block by row block (row block bm starts at column block floor(bm BM / BN)), so
+// the CTAs share out only tiles with work.
+__device__ __forceinline__ void tile_at(int u, int mt, int nt, int sym, int& m0, int& n0) {
   if (sym) {
     for (int bm = 0; bm < mt; ++bm) {
       const int f = (bm * BM) / BN, cnt = nt > f ? nt - f : 0;
@@ -246,17 +245,14 @@ __device__ __forceinline__ void tile_at(int u, bool rows_first, int mt, int nt, 
     m0 = n0 = 0;  // not reached: u < the launcher's tile count
     return;
   }
-  const int bm = rows_first ? u % mt : u / nt, bn = rows_first ? u / mt : u % nt;
-  m0 = bm * BM;
-  n0 = bn * BN;
+  m0 = (u / nt) * BM;
+  n0 = (u % nt) * BN;
 }
 
-// tmA / tmB: K-major boxes of 64 columns x BM / BN rows (B_MN: 64 x 64 boxes of
-// the K x N operand).  With a_sym / b_sym, tmAt / tmBt address the same matrices
-// in 64 x 64 boxes for the transposed (MN-major) reads of the k-blocks whose
-// tiles were not stored: a 128-row A box or 256-row B box of one k-block is
-// either stored whole or not at all.
-template <bool B_MN>
+// tmA / tmB: K-major boxes of 64 columns x BM / BN rows.  With a_sym / b_sym,
+// tmAt / tmBt address the same matrices in 64 x 64 boxes for the transposed
+// (MN-major) reads of the k-blocks whose tiles were not stored: a 128-row A box
+// or 256-row B box of one k-block is either stored whole or not at all.
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_p(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmBt, GemmArgs g) {
@@ -297,7 +293,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
       int m0, n0;
-      tile_at(t, B_MN, mt, nt, g.sym, m0, n0);
+      tile_at(t, mt, nt, g.sym, m0, n0);
       for (int kb = 0; kb < nk; ++kb, ++it) {
         const int s = int(it % STAGES);
         if (!mbar_wait(empty_bar(s), ((it / STAGES) & 1u) ^ 1u, g.status, 1)) {
@@ -313,11 +309,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         } else {
           tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
         }
-        if (B_MN) {
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(b_dst + uint32_t(j) * (BK * 128), &tmB, n0 + 64 * j, kb * BK, full_bar(s));
-        } else if (g.b_sym && !sym_stored(n0, kb * BK)) {  // read transposed (MN-major), like B_MN
+        if (g.b_sym && !sym_stored(n0, kb * BK)) {  // read transposed (MN-major): four 64-row boxes
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
             tma_load_2d(b_dst + uint32_t(j) * (BK * 128), &tmBt, n0 + 64 * j, kb * BK, full_bar(s));
@@ -335,7 +327,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
       int m0, n0;
-      tile_at(t, B_MN, mt, nt, g.sym, m0, n0);
+      tile_at(t, mt, nt, g.sym, m0, n0);
       const int buf = int(tc & 1u);
       if (tc >= 2 && !mbar_wait(tempty_bar(buf), ((tc >> 1) & 1u) ^ 1u, g.status, 5)) break;
       tc_fence_after();
@@ -350,7 +342,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t a_addr = base + uint32_t(s) * STAGE_BYTES;
         const uint32_t b_addr = a_addr + A_STAGE;
         const bool a_t = g.a_sym && !sym_stored(m0, kb * BK);
-        const bool b_t = B_MN || (g.b_sym && !sym_stored(n0, kb * BK));
+        const bool b_t = g.b_sym && !sym_stored(n0, kb * BK);
         const uint32_t id = idesc_bf16(BM, BN, b_t ? 1 : 0, a_t ? 1 : 0);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
@@ -376,7 +368,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t tc = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       int m0, n0;
-      tile_at(t, B_MN, mt, nt, g.sym, m0, n0);
+      tile_at(t, mt, nt, g.sym, m0, n0);
       const int buf = int(tc & 1u);
       const bool ok = mbar_wait(tfull_bar(buf), (tc >> 1) & 1u, g.status, 4);
       tc_fence_after();
@@ -394,6 +386,248 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS_P);
+  }
+}
+
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+// B X on pairs of CTAs (clusters of two): one 256 x 256 output tile per pair.
+// Each CTA stages 128 rows of the A operand and 128 columns of X for a k-block
+// (32 KB instead of the single-CTA kernel's 48 KB), the pair's first CTA (the
+// leader) issues M = 256 products that read both CTAs' shared memory, and each
+// CTA's tensor memory receives its own 128 accumulator rows.  Half the shared
+// memory per stage leaves room for six stages: more copies in flight for the same
+// tensor-core work, and a third less L2 traffic.
+// Barriers: the leader's `full` (both CTAs' copies complete their bytes on it),
+// each CTA's `empty` and `tfull` (the leader's commits reach both CTAs), the
+// leader's `tempty` (the epilogue warps of both CTAs arrive).  Every wait is
+// bounded; a cluster barrier keeps either CTA from freeing its tensor memory or
+// exiting while the pair's products may still use it.
+constexpr int PM = 256, STAGES2 = 6;
+constexpr int HALF_STAGE = 128 * BK * 2;       // 128 rows (or columns) x 64 bf16: 16 KB
+constexpr int STAGE2_BYTES = 2 * HALF_STAGE;   // one CTA's part of a k-block
+constexpr int GEMM2_SMEM = STAGES2 * STAGE2_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// the shared::cluster address of `addr` (a shared::cta address) in CTA `rank`
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(addr), "r"(rank));
+  return a;
+}
+
+// every thread of both CTAs
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// bounded wait on a barrier that the other CTA of the pair also arrives on
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* status, int code) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    if ((it & 255) == 255 && clock64() - t0 > kWaitCycles) {
+      if (status) atomicExch(status, code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// a box into this CTA's shared memory, its bytes completed on `cluster_bar`
+// (a barrier of either CTA of the pair)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(cluster_bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// arrive on the barrier at this shared::cta offset in both CTAs once the products
+// issued so far have completed
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  const uint16_t both = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(both)
+      : "memory");
+}
+
+// made collectively by one warp of each CTA of the pair: the same columns in both
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D = alpha * (A B) + beta * C with B given as [K x N] N-contiguous (tmB: 64 x 64
+// boxes) and A K-major (tmA: boxes of 64 columns x 128 rows; with a_sym, tmAt's
+// 64 x 64 boxes give the transposed reads of A's k-blocks below its stored
+// tiles).  Pairs walk the 256 x 256 tiles t = cluster, + clusters, ..., row
+// blocks fastest.  A pair tile's rows start at a multiple of 256, so its two
+// 128-row halves of a k-block are stored or transposed together and one
+// instruction descriptor serves both.
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm_2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const __grid_constant__ CUtensorMap tmAt, GemmArgs g) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  const uint32_t bar_base = base + STAGES2 * STAGE2_BYTES;
+  auto full_bar = [&](int s) { return bar_base + 8u * uint32_t(s); };
+  auto empty_bar = [&](int s) { return bar_base + 8u * uint32_t(STAGES2 + s); };
+  auto tfull_bar = [&](int b) { return bar_base + 8u * uint32_t(2 * STAGES2 + b); };
+  auto tempty_bar = [&](int b) { return bar_base + 8u * uint32_t(2 * STAGES2 + 2 + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES2 * STAGE2_BYTES + 8 * (2 * STAGES2 + 4));
+
+  const uint32_t rank = cluster_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = (g.M + PM - 1) / PM, ntiles = g.ntiles;
+  const int nk = (g.K + BK - 1) / BK;
+  const int pair = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(full_bar(s), 1);   // the leader's expect_tx
+      mbar_init(empty_bar(s), 1);  // the leader's commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * EPI_WARPS);  // the epilogue warps of both CTAs
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS_P);
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers exist and the columns are held before any remote use
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer (both CTAs: this CTA's halves)
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = pair; ok && t < ntiles; t += npairs) {
+      const int ma = (t % mt) * PM + 128 * int(rank), nb = (t / mt) * PM + 128 * int(rank);
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = int(it % STAGES2);
+        if (!mbar_wait(empty_bar(s), ((it / STAGES2) & 1u) ^ 1u, g.status, 11)) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_dst = base + uint32_t(s) * STAGE2_BYTES;
+        const uint32_t b_dst = a_dst + HALF_STAGE;
+        const uint32_t fb = map_rank(full_bar(s), 0);
+        if (rank == 0) mbar_expect_tx(full_bar(s), 2 * STAGE2_BYTES);
+        if (g.a_sym && !sym_stored(ma, kb * BK)) {
+          tma_load_2d_pair(a_dst, &tmAt, ma, kb * BK, fb);
+          tma_load_2d_pair(a_dst + uint32_t(BK * 128), &tmAt, ma + 64, kb * BK, fb);
+        } else {
+          tma_load_2d_pair(a_dst, &tmA, kb * BK, ma, fb);
+        }
+        tma_load_2d_pair(b_dst, &tmB, nb, kb * BK, fb);
+        tma_load_2d_pair(b_dst + uint32_t(BK * 128), &tmB, nb + 64, kb * BK, fb);
+      }
+    }
+    // drain (leader): the pair's last copies have landed; the peer waits for this
+    // at the closing cluster barrier
+    if (rank == 0)
+      for (uint32_t d = it > uint32_t(STAGES2) ? it - STAGES2 : 0; d < it; ++d)
+        mbar_wait(full_bar(int(d % STAGES2)), (d / STAGES2) & 1u, g.status, 12);
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (leader)
+    uint32_t it = 0, tc = 0;
+    bool ok = true;
+    for (int t = pair; ok && t < ntiles; t += npairs) {
+      const int m0 = (t % mt) * PM;
+      const int buf = int(tc & 1u);
+      if (tc >= 2 && !mbar_wait_cluster(tempty_bar(buf), ((tc >> 1) & 1u) ^ 1u, g.status, 15)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + uint32_t(buf) * BN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = int(it % STAGES2);
+        if (!mbar_wait(full_bar(s), (it / STAGES2) & 1u, g.status, 13)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = base + uint32_t(s) * STAGE2_BYTES;
+        const uint32_t b_addr = a_addr + HALF_STAGE;
+        const bool a_t = g.a_sym && !sym_stored(m0, kb * BK);
+        const uint32_t id = idesc_bf16(PM, BN, 1, a_t ? 1 : 0);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = a_t ? sdesc(a_addr + uint32_t(kk) * 16u * 128u, BK * 128, 1024)
+                                  : sdesc(a_addr + 32u * kk, 16, 1024);
+          const uint64_t bd = sdesc(b_addr + uint32_t(kk) * 16u * 128u, BK * 128, 1024);
+          mma_bf16_pair(acc, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit_pair(empty_bar(s));
+      }
+      if (!ok) break;
+      mma_commit_pair(tfull_bar(buf));
+      ++tc;
+    }
+    if (tc > 0) mbar_wait(tfull_bar(int((tc - 1) & 1u)), ((tc - 1) >> 1) & 1u, g.status, 16);
+  } else if (warp >= 2) {
+    // ---------------- epilogue (both CTAs: this CTA's 128 rows of the tile)
+    const int q = warp & 3;
+    const uint32_t te0 = map_rank(tempty_bar(0), 0), te1 = map_rank(tempty_bar(1), 0);
+    uint32_t tc = 0;
+    for (int t = pair; t < ntiles; t += npairs) {
+      const int m0 = (t % mt) * PM + 128 * int(rank), n0 = (t / mt) * PM;
+      const int buf = int(tc & 1u);
+      const bool ok = mbar_wait(tfull_bar(buf), (tc >> 1) & 1u, g.status, 14);
+      tc_fence_after();
+      if (!ok) break;
+      const int half = (warp - 2) >> 2;
+      epilogue_tile(g, tmem, uint32_t(buf) * BN, m0, n0, q, lane, half * (BN / 64), (half + 1) * (BN / 64));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(buf ? te1 : te0);
+      ++tc;
+    }
+  }
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS_P);
   }
 }
 
@@ -603,13 +837,19 @@ int check_mat(const bq_mat& t) {
   return BQ_OK;
 }
 
-int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tat, const CUtensorMap& tbt,
+// the GEMM kernels' shared-memory attributes, set once per device (they belong
+// to the current device)
+int gemm_attrs() {
+  if (once_per_device(kOnceGemmAttr) &&
+      (cudaFuncSetAttribute(k_gemm_p, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) != cudaSuccess ||
+       cudaFuncSetAttribute(k_gemm_2, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM2_SMEM) != cudaSuccess))
+    return check("bq_muon_ns (gemm shared memory attributes)");
+  return BQ_OK;
+}
+
+int gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tat, const CUtensorMap& tbt,
          const GemmArgs& g, cudaStream_t s) {
-  if (once_per_device(kOnceGemmAttr)) {  // the attribute belongs to the current device
-    if (cudaFuncSetAttribute(k_gemm_p<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(k_gemm_p<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) != cudaSuccess)
-      return check("bq_muon_ns (gemm shared memory attribute)");
-  }
+  if (int rc = gemm_attrs()) return rc;
   const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN;
   GemmArgs a = g;
   a.ntiles = mt * nt;
@@ -619,11 +859,62 @@ int gemm(bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
   }
   if (a.ntiles == 0) return BQ_OK;
   const unsigned grid = unsigned(std::min(a.ntiles, sm_count()));
-  if (b_mn)
-    k_gemm_p<true><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, tat, tbt, a);
-  else
-    k_gemm_p<false><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, tat, tbt, a);
+  k_gemm_p<<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, tat, tbt, a);
   return check("bq_muon_ns (gemm)");
+}
+
+// Clusters of two k_gemm_2 CTAs that fit the device at once (cached per device;
+// half the SMs if the occupancy query fails)
+int pair_slots() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sm_count() / 2;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(2 * sm_count()));
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = GEMM2_SMEM;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_2, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = sm_count() / 2;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// B X on CTA pairs: A K-major (ta; tat for the transposed k-blocks of a symmetric
+// A), B [K x N] N-contiguous (tb)
+int gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tat, const GemmArgs& g,
+              cudaStream_t s) {
+  if (int rc = gemm_attrs()) return rc;
+  GemmArgs a = g;
+  a.ntiles = ((g.M + PM - 1) / PM) * ((g.N + PM - 1) / PM);
+  if (a.ntiles == 0) return BQ_OK;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(unsigned(2 * std::min(a.ntiles, pair_slots())));
+  cfg.blockDim = dim3(GEMM_THREADS);
+  cfg.dynamicSmemBytes = GEMM2_SMEM;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_gemm_2, ta, tb, tat, a) != cudaSuccess) return check("bq_muon_ns (pair gemm)");
+  return check("bq_muon_ns (pair gemm)");
 }
 
 // Matrix i's workspace region in the concurrent layout starts at region_off[i]
@@ -679,13 +970,13 @@ int ns_one(const bq_mat& t, unsigned char* w, int* status, int steps, float a, f
     const int nxt = cur ^ 1;
     // A = X X^T (symmetric: the tiles touching the upper triangle)
     GemmArgs g1{int(p.m), int(p.m), int(p.n), 1.f, 0.f, nullptr, A, 0, p.lda, status, kSymmetric, 0, 0, 0};
-    if (int rc = gemm(false, mXa[cur], mXb[cur], mXa[cur], mXa[cur], g1, s)) return rc;
+    if (int rc = gemm(mXa[cur], mXb[cur], mXa[cur], mXa[cur], g1, s)) return rc;
     // B = c (A A^T) + b A   (A symmetric and stored as such: both operands read it)
     GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric, 0, kSymmetric, kSymmetric};
-    if (int rc = gemm(false, mAa, mAb, mAmn, mAmn, g2, s)) return rc;
+    if (int rc = gemm(mAa, mAb, mAmn, mAmn, g2, s)) return rc;
     // X' = B X + a X   (B symmetric and stored as such)
     GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0, 0, kSymmetric, 0};
-    if (int rc = gemm(true, mBa, mXmn[cur], mBmn, mBmn, g3, s)) return rc;
+    if (int rc = gemm_pair(mBa, mXmn[cur], mBmn, g3, s)) return rc;
     cur = nxt;
   }
   // y = X (transposed back for a tall input)

@@ -289,6 +289,10 @@ int bq_quant_fp8(const bq_shard* shard, const float* master, uint8_t* fp8_out, f
  * device's side streams).  Any ws_bytes of at least the largest single
  * matrix's need also works: the matrices then run one after another on
  * `stream` and reuse one region.  The results are the same either way.
+ * Resources: every CTA of the products holds all 512 tensor-memory columns of
+ * its SM while it runs (the B X product runs on clusters of two CTAs that hold
+ * the columns of both their SMs); a CTA whose columns are held by a co-resident
+ * kernel waits until that kernel's CTA exits.
  * Errors: BQ_EINVAL (bad descriptor, rows or cols above 2^20), BQ_EALIGN,
  * BQ_ENOSPC, BQ_EDEVICE (driver entry point for tensor maps unavailable). */
 int bq_muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes);
