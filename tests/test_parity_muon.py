@@ -29,6 +29,9 @@ def test_one_step(cuda):
     [(256, 256), (256, 640), (640, 256)],   # several tiles, tall input transposed
     [(200, 328), (328, 200), (72, 1000)],   # ragged edges in every dimension
     [(512, 1536)],
+    # B X on CTA pairs (256-row tiles, 128 rows a CTA): the last pair tile ragged in
+    # one CTA or wholly past the matrix in the other, N ragged too
+    [(700, 900), (1100, 640), (300, 2000)],
 ])
 def test_five_steps(cuda, shapes):
     errs = run_muon_case(cuda, shapes, steps=5)
