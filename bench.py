@@ -397,6 +397,23 @@ class E2EPipeline:
             self.ev_down[j].record(self.down)
         self.k += 1
 
+    def link(self, comp, reps=3):
+        """The host link on this machine, each direction alone: the step's upload and
+        its read-back as single copies (best of reps), in ms."""
+        torch = self.torch
+        best = [float("inf"), float("inf")]
+        for _ in range(reps):
+            for k, (dst, src) in enumerate(((self.gbufs[0], self.host_grads), (self.host_fp8, self.fp8[0]))):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(comp)
+                with torch.cuda.stream(comp):
+                    dst.copy_(src, non_blocking=True)
+                e1.record(comp)
+                torch.cuda.synchronize()
+                best[k] = min(best[k], e0.elapsed_time(e1))
+        return best
+
     def measure(self, comp, steps, warmup=3):
         torch = self.torch
         for _ in range(warmup):
@@ -828,6 +845,8 @@ def run_ours(args):
     pipe = E2EPipeline(step, dev)
     e2e_ms = pipe.measure(stream, steps=max(5, args.steps // 4))
     h2d, d2h = pipe.h2d, pipe.d2h
+    link_ms = pipe.link(stream)
+    pipe_h2d_bytes, pipe_fp8_bytes = pipe.h2d, pipe.host_fp8.numel()
     del pipe
     torch.cuda.empty_cache()
     muon_e2e = None
@@ -905,7 +924,12 @@ def run_ours(args):
             "e2e": {"value": round(job_throughput(B, world, e2e_max) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "overlap": "upload of step k+1 and read-back of step k run on their own streams during step k",
-                    "ms_per_step": round(e2e_max, 4)},
+                    "ms_per_step": round(e2e_max, 4),
+                    "link": {"h2d_GB/s": round(gbs(pipe_h2d_bytes, link_ms[0]), 1),
+                             "d2h_GB/s": round(gbs(pipe_fp8_bytes, link_ms[1]), 1),
+                             "note": "the host link measured on this box after the timed steps, each direction "
+                                     "alone (the gradient upload; the FP8 buffer's read-back); both directions "
+                                     "at once share it"}},
             "gpu_launches": args.steps * (head["launches"] + (muon_launches(muon) if muon else 0)),
             "clocks": clk,
         }
