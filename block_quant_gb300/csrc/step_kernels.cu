@@ -13,7 +13,8 @@
 //                  the tile's inputs kept in tensor memory between its phases
 //   k_tile32       8-bit Adam with the walkthrough's 32x32 state tiles (same
 //                  tensor-memory scheme)
-//   k_quant_*      standalone FP8 requantisation
+//   k_quant_*      FP8 requantisation on its own: standalone, and for the
+//                  tiles of bands whose Adam ran as flat pieces
 //   k_dequant_*    the bf16 view (code x tile scale) of the gathered FP8 buffer
 //   k_muon_*       Muon's momentum + gather and apply around Newton-Schulz
 // The 8-bit Adam is the pages' block-quantised optimizer state kept local to a
@@ -1300,6 +1301,69 @@ __global__ void __launch_bounds__(kThreads) k_quant_region(const RegionGroup* __
   }
 }
 
+// FP8 tiles (<= 128 x 128: the band-tile and tile lists) in two passes: the
+// first reads the tile, reduces max|p'| and keeps rows 0-63 in shared memory
+// (32 KB); the second converts those from shared memory and re-reads only rows
+// 64-127 (from L2), so half as many lines must stay in L2 between the passes.
+constexpr int kHalfVecs = 64 * 16;  // 8-element vectors in rows 0-63 of a 128-column tile
+constexpr int kQuantTileCtas = 6;   // 197 KB of shared memory per SM (32 rows: 8 CTAs, 96 rows: 4 were slower)
+
+__global__ void __launch_bounds__(kThreads) k_quant_tile(const RegionGroup* __restrict__ groups, int ngroups,
+                                                         const float* __restrict__ master, uint8_t* __restrict__ fp8,
+                                                         float* __restrict__ fp8_scale) {
+  __shared__ float4 s_half[2 * kHalfVecs];  // vector v's halves at v and kHalfVecs + v
+  __shared__ uint32_t red[kWarps];
+  __shared__ QScale s_q;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
+    const RegionGroup g = groups[gi];
+    if (g.fslot < 0) continue;  // uniform per CTA
+    const int vpr = g.width >> 3, nvec = g.rows * vpr, nlow = min(nvec, 64 * vpr);
+    uint32_t ap = 0;
+    for (int v = threadIdx.x; v < nvec; v += kThreads) {
+      const int r = vec_row(v, vpr), k = v - r * vpr;
+      const int64_t pos = g.pos + int64_t(r) * g.C + (k << 3);
+      const float4 p0 = *reinterpret_cast<const float4*>(master + pos);
+      const float4 p1 = *reinterpret_cast<const float4*>(master + pos + 4);
+      if (v < nlow) {
+        s_half[v] = p0;
+        s_half[kHalfVecs + v] = p1;
+      }
+      ap = max(ap, max(max(__float_as_uint(fabsf(p0.x)), __float_as_uint(fabsf(p0.y))),
+                       max(__float_as_uint(fabsf(p0.z)), __float_as_uint(fabsf(p0.w)))));
+      ap = max(ap, max(max(__float_as_uint(fabsf(p1.x)), __float_as_uint(fabsf(p1.y))),
+                       max(__float_as_uint(fabsf(p1.z)), __float_as_uint(fabsf(p1.w)))));
+    }
+    ap = __reduce_max_sync(0xFFFFFFFFu, ap);
+    if (lane == 0) red[warp] = ap;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t t = __reduce_max_sync(0xFFFFFFFFu, lane < kWarps ? red[lane] : 0u);
+      if (lane == 0) {
+        s_q = qscale(t, 448.f);
+        fp8_scale[g.fslot] = s_q.s;
+      }
+    }
+    __syncthreads();
+    const QScale q = s_q;
+    for (int v = threadIdx.x; v < nvec; v += kThreads) {
+      const int r = vec_row(v, vpr), k = v - r * vpr;
+      const int64_t pos = g.pos + int64_t(r) * g.C + (k << 3);
+      float4 p0, p1;
+      if (v < nlow) {
+        p0 = s_half[v];
+        p1 = s_half[kHalfVecs + v];
+      } else {
+        p0 = *reinterpret_cast<const float4*>(master + pos);
+        p1 = *reinterpret_cast<const float4*>(master + pos + 4);
+      }
+      const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      *reinterpret_cast<uint2*>(fp8 + pos) = codes_e4m3(pv, q);
+    }
+    __syncthreads();  // s_half, red and s_q are reused by the next tile
+  }
+}
+
 // ---------------------------------------------------------------- the bf16 view after the AllGather
 // Compute reads each gathered FP8 parameter as code x tile scale: the E4M3 code
 // decoded exactly (every E4M3 value is a half), times the fp32 scale (one fp32
@@ -1443,8 +1507,8 @@ int launch_adam8(const DevTables& t, const AdamArgs& a, void* stream) {
   }
   if (fp8 && t.n_band_tiles) {
     // FP8 of tensors whose Adam ran as band pieces: two passes per tile over the
-    // just-written master (L2)
-    k_quant_region<<<std::min(t.n_band_tiles, sms * 8), kThreads, 2 * sizeof(uint32_t), s>>>(
+    // just-written master, half the tile held on chip between them
+    k_quant_tile<<<std::min(t.n_band_tiles, sms * kQuantTileCtas), kThreads, 0, s>>>(
         t.band_tiles, t.n_band_tiles, a.master, a.fp8, a.fp8_scale);
     if (int rc = check_launch("bq_step_adam8 (band FP8 tiles)")) return rc;
   }
@@ -1482,13 +1546,13 @@ int launch_quant_fp8(const DevTables& t, const float* master, uint8_t* fp8, floa
     if (int rc = check_launch("bq_quant_fp8 (strips)")) return rc;
   }
   if (t.n_band_tiles) {
-    k_quant_region<<<std::min(t.n_band_tiles, sms * 8), kThreads, 2 * sizeof(uint32_t), s>>>(
-        t.band_tiles, t.n_band_tiles, master, fp8, fp8_scale);
+    k_quant_tile<<<std::min(t.n_band_tiles, sms * kQuantTileCtas), kThreads, 0, s>>>(t.band_tiles, t.n_band_tiles,
+                                                                                     master, fp8, fp8_scale);
     if (int rc = check_launch("bq_quant_fp8 (band tiles)")) return rc;
   }
   if (t.n_tiles) {
-    k_quant_region<<<std::min(t.n_tiles, sms * kTileCtasPerSm), kThreads, 2 * sizeof(uint32_t), s>>>(
-        t.tiles, t.n_tiles, master, fp8, fp8_scale);
+    k_quant_tile<<<std::min(t.n_tiles, sms * kQuantTileCtas), kThreads, 0, s>>>(t.tiles, t.n_tiles, master, fp8,
+                                                                                fp8_scale);
     if (int rc = check_launch("bq_quant_fp8 (tiles)")) return rc;
   }
   return BQ_OK;
