@@ -843,7 +843,9 @@ def run_ours(args):
     # gradients uploaded, pack + Adam + FP8, the FP8 staging buffer and scales
     # read back; uploads and read-backs overlap the neighbouring steps' kernels
     pipe = E2EPipeline(step, dev)
-    e2e_ms = pipe.measure(stream, steps=max(5, args.steps // 4))
+    # as many steps as the timed region, so that filling and draining the
+    # upload / read-back pipeline is spread over the same count
+    e2e_ms = pipe.measure(stream, steps=args.steps)
     h2d, d2h = pipe.h2d, pipe.d2h
     link_ms = pipe.link(stream)
     pipe_h2d_bytes, pipe_fp8_bytes = pipe.h2d, pipe.host_fp8.numel()
@@ -852,7 +854,7 @@ def run_ours(args):
     muon_e2e = None
     if muon:
         muon.pin_host()
-        muon_e2e = muon.measure_e2e(stream)
+        muon_e2e = muon.measure_e2e(stream, steps=args.steps)
 
     extra = {}
     side = torch.cuda.Stream(dev)
