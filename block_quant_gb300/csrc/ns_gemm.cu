@@ -96,6 +96,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// c MN-major 64 x 64 chunks in one copy: a 3-D map {64 columns, rows, 64-column
+// chunks} (chunk stride 128 bytes) lands them 8 KB apart, the layout of c
+// separate 64 x 64 boxes
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int row, int chunk, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(chunk), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
@@ -304,15 +315,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t b_dst = a_dst + A_STAGE;
         mbar_expect_tx(full_bar(s), STAGE_BYTES);
         if (g.a_sym && !sym_stored(m0, kb * BK)) {  // rows m0.. of the k-block, read as its transpose (MN-major)
-          tma_load_2d(a_dst, &tmAt, m0, kb * BK, full_bar(s));
-          tma_load_2d(a_dst + uint32_t(BK * 128), &tmAt, m0 + 64, kb * BK, full_bar(s));
+          tma_load_3d(a_dst, &tmAt, kb * BK, m0 / 64, full_bar(s));  // two 64-row chunks
         } else {
           tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
         }
-        if (g.b_sym && !sym_stored(n0, kb * BK)) {  // read transposed (MN-major): four 64-row boxes
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(b_dst + uint32_t(j) * (BK * 128), &tmBt, n0 + 64 * j, kb * BK, full_bar(s));
+        if (g.b_sym && !sym_stored(n0, kb * BK)) {  // read transposed (MN-major): four 64-row chunks
+          tma_load_3d(b_dst, &tmBt, kb * BK, n0 / 64, full_bar(s));
         } else {
           tma_load_2d(b_dst, &tmB, kb * BK, n0, full_bar(s));
         }
@@ -464,6 +472,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int row, int chunk,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(chunk), "r"(cluster_bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                               uint32_t accumulate) {
   asm volatile(
@@ -555,13 +572,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t fb = map_rank(full_bar(s), 0);
         if (rank == 0) mbar_expect_tx(full_bar(s), 2 * STAGE2_BYTES);
         if (g.a_sym && !sym_stored(ma, kb * BK)) {
-          tma_load_2d_pair(a_dst, &tmAt, ma, kb * BK, fb);
-          tma_load_2d_pair(a_dst + uint32_t(BK * 128), &tmAt, ma + 64, kb * BK, fb);
+          tma_load_3d_pair(a_dst, &tmAt, kb * BK, ma / 64, fb);  // two 64-row chunks
         } else {
           tma_load_2d_pair(a_dst, &tmA, kb * BK, ma, fb);
         }
-        tma_load_2d_pair(b_dst, &tmB, nb, kb * BK, fb);
-        tma_load_2d_pair(b_dst + uint32_t(BK * 128), &tmB, nb + 64, kb * BK, fb);
+        tma_load_3d_pair(b_dst, &tmB, kb * BK, nb / 64, fb);  // two 64-column chunks of X
       }
     }
     // drain (leader): the pair's last copies have landed; the peer waits for this
@@ -791,6 +806,25 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int6
   return BQ_OK;
 }
 
+// The same matrix as MN-major chunks: {64 columns, rows, ceil(cols / 64) chunks}
+// with the chunk stride 128 bytes, boxes of 64 x 64 x `chunks` (a copy brings
+// that many consecutive 64-column chunks of 64 rows).  Columns past `cols` inside
+// the last chunk come from the row padding: they only reach output rows or
+// columns past the matrix, which are never stored; rows past `rows` read as 0.
+int make_map3(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows, int64_t ld, int chunks) {
+  EncodeTiled enc = encoder();
+  if (!enc) return set_error(BQ_EDEVICE, "bq_muon_ns: cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[3] = {64u, cuuint64_t(rows), cuuint64_t((cols + 63) / 64)};
+  const cuuint64_t strides[2] = {cuuint64_t(ld) * 2, 128u};
+  const cuuint32_t box[3] = {64u, 64u, cuuint32_t(chunks)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(BQ_EINVAL, "bq_muon_ns: tensor map encoding failed (" + std::to_string(int(r)) + ")");
+  return BQ_OK;
+}
+
 int64_t pitch_of(int64_t cols) { return (cols + 63) / 64 * 64; }  // 128-byte rows
 
 struct NsPlan {
@@ -951,19 +985,23 @@ int ns_one(const bq_mat& t, unsigned char* w, int* status, int steps, float a, f
   k_scale_copy<<<cg, 256, 0, s>>>(x, t.rows, t.cols, t.ld_x, X0, p.ldx, p.tall ? 1 : 0, inv);
   if (int rc = check("bq_muon_ns (scale)")) return rc;
 
-  // tensor maps: X as K-major A operand / K-major B operand / MN-major B operand, A, B
-  CUtensorMap mXa[2], mXb[2], mXmn[2], mAa, mAb, mAmn, mBa, mBmn;
+  // tensor maps: X as K-major A operand / K-major B operand / MN-major B operand
+  // (two 64-column chunks a copy: a pair CTA's 128 columns), A and B K-major, and
+  // A, B as MN-major chunks for the transposed reads (two chunks: a 128-row A
+  // operand box; four: a 256-row B operand box)
+  CUtensorMap mXa[2], mXb[2], mXmn[2], mAa, mAb, mAmn2, mAmn4, mBa, mBmn2;
   __nv_bfloat16* Xs[2] = {X0, X1};
   for (int j = 0; j < 2; ++j) {
     if (int rc = make_map(&mXa[j], Xs[j], p.n, p.m, p.ldx, BM)) return rc;
     if (int rc = make_map(&mXb[j], Xs[j], p.n, p.m, p.ldx, BN)) return rc;
-    if (int rc = make_map(&mXmn[j], Xs[j], p.n, p.m, p.ldx, BK)) return rc;
+    if (int rc = make_map3(&mXmn[j], Xs[j], p.n, p.m, p.ldx, 2)) return rc;
   }
   if (int rc = make_map(&mAa, A, p.m, p.m, p.lda, BM)) return rc;
   if (int rc = make_map(&mAb, A, p.m, p.m, p.lda, BN)) return rc;
-  if (int rc = make_map(&mAmn, A, p.m, p.m, p.lda, BK)) return rc;  // 64 x 64 boxes: transposed reads
+  if (int rc = make_map3(&mAmn2, A, p.m, p.m, p.lda, 2)) return rc;
+  if (int rc = make_map3(&mAmn4, A, p.m, p.m, p.lda, 4)) return rc;
   if (int rc = make_map(&mBa, B, p.m, p.m, p.lda, BM)) return rc;
-  if (int rc = make_map(&mBmn, B, p.m, p.m, p.lda, BK)) return rc;
+  if (int rc = make_map3(&mBmn2, B, p.m, p.m, p.lda, 2)) return rc;
 
   int cur = 0;
   for (int it = 0; it < steps; ++it) {
@@ -973,10 +1011,10 @@ int ns_one(const bq_mat& t, unsigned char* w, int* status, int steps, float a, f
     if (int rc = gemm(mXa[cur], mXb[cur], mXa[cur], mXa[cur], g1, s)) return rc;
     // B = c (A A^T) + b A   (A symmetric and stored as such: both operands read it)
     GemmArgs g2{int(p.m), int(p.m), int(p.m), c, b, A, B, p.lda, p.lda, status, kSymmetric, 0, kSymmetric, kSymmetric};
-    if (int rc = gemm(mAa, mAb, mAmn, mAmn, g2, s)) return rc;
+    if (int rc = gemm(mAa, mAb, mAmn2, mAmn4, g2, s)) return rc;
     // X' = B X + a X   (B symmetric and stored as such)
     GemmArgs g3{int(p.m), int(p.n), int(p.m), 1.f, a, Xs[cur], Xs[nxt], p.ldx, p.ldx, status, 0, 0, kSymmetric, 0};
-    if (int rc = gemm_pair(mBa, mXmn[cur], mBmn, g3, s)) return rc;
+    if (int rc = gemm_pair(mBa, mXmn[cur], mBmn2, g3, s)) return rc;
     cur = nxt;
   }
   // y = X (transposed back for a tall input)
