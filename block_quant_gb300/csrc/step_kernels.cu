@@ -599,31 +599,52 @@ __device__ __forceinline__ void strip_producer(const RegionGroup* __restrict__ g
         if (!ok) break;
       }
       TmaStage& S = ring[s];
-      // pass q, lane = 4 w + arr: array arr (g, p, m, v) of the stage's block 8 q + w
-      constexpr int kPasses = (kCons + 7) / 8;
-      bool staged[kPasses];
-      int64_t start[kPasses];
-      uint32_t nst = 0;
-#pragma unroll
-      for (int q = 0; q < kPasses; ++q) {
-        const int w = 8 * q + (lane >> 2);
-        int nel = 0, slot = 0;
-        start[q] = 0;
-        const bool have = w < kCons && j + w < nblk;
-        if (have) region_block(g, j + w, start[q], nel, slot);
-        staged[q] = have && block_staged(start[q], nel);
-        nst += __popc(__ballot_sync(0xFFFFFFFFu, staged[q] && (lane & 3) == 0));
+      // a flat piece's blocks lie one after another in every array: a stage of
+      // kCons full, aligned blocks is one bulk copy per array (4 copies instead of
+      // 4 kCons; the copy engine's cost is per copy as much as per byte)
+      bool merged = false;
+      int64_t first = 0;
+      if (g.width == g.C && j + kCons <= nblk) {
+        int64_t last;
+        int nf, nl, sf, sl;
+        region_block(g, j, first, nf, sf);
+        region_block(g, j + kCons - 1, last, nl, sl);
+        merged = block_staged(first, nf) && nl == 256;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], nst * kBlockBytes);
-      __syncwarp();
+      if (merged) {
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], kCons * kBlockBytes);
+        __syncwarp();
+        if (lane == 0) bulk_load(S.g[0], a.grad + first, 512 * kCons, &full[s]);
+        else if (lane == 1) bulk_load(S.p[0], a.master + first, 1024 * kCons, &full[s]);
+        else if (lane == 2) bulk_load(S.m[0], a.m + first, 256 * kCons, &full[s]);
+        else if (lane == 3) bulk_load(S.v[0], a.v + first, 256 * kCons, &full[s]);
+      } else {
+        // pass q, lane = 4 w + arr: array arr (g, p, m, v) of the stage's block 8 q + w
+        constexpr int kPasses = (kCons + 7) / 8;
+        bool staged[kPasses];
+        int64_t start[kPasses];
+        uint32_t nst = 0;
 #pragma unroll
-      for (int q = 0; q < kPasses; ++q) {
-        const int w = 8 * q + (lane >> 2), arr = lane & 3;
-        if (staged[q]) {
-          if (arr == 0) bulk_load(S.g[w], a.grad + start[q], 512, &full[s]);
-          else if (arr == 1) bulk_load(S.p[w], a.master + start[q], 1024, &full[s]);
-          else if (arr == 2) bulk_load(S.m[w], a.m + start[q], 256, &full[s]);
-          else bulk_load(S.v[w], a.v + start[q], 256, &full[s]);
+        for (int q = 0; q < kPasses; ++q) {
+          const int w = 8 * q + (lane >> 2);
+          int nel = 0, slot = 0;
+          start[q] = 0;
+          const bool have = w < kCons && j + w < nblk;
+          if (have) region_block(g, j + w, start[q], nel, slot);
+          staged[q] = have && block_staged(start[q], nel);
+          nst += __popc(__ballot_sync(0xFFFFFFFFu, staged[q] && (lane & 3) == 0));
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], nst * kBlockBytes);
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < kPasses; ++q) {
+          const int w = 8 * q + (lane >> 2), arr = lane & 3;
+          if (staged[q]) {
+            if (arr == 0) bulk_load(S.g[w], a.grad + start[q], 512, &full[s]);
+            else if (arr == 1) bulk_load(S.p[w], a.master + start[q], 1024, &full[s]);
+            else if (arr == 2) bulk_load(S.m[w], a.m + start[q], 256, &full[s]);
+            else bulk_load(S.v[w], a.v + start[q], 256, &full[s]);
+          }
         }
       }
       // scale i (i & 1 ? v : m of block i >> 1) by lane i % 32
