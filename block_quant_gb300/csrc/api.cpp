@@ -3,6 +3,7 @@
 // checks arguments, builds integer work tables and launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -56,6 +57,12 @@ struct bq_shard {
   int64_t total;           // elements of the shard range
   int64_t nm, nf;          // Adam / FP8 scale slots of the range
   DevTables dev;
+  // the strips' tensor maps in the workspace hold the buffers of the last step
+  // that wrote them (key); they are rebuilt when the buffers change
+  std::vector<MapInterval> maps;
+  mutable std::mutex map_mu;
+  mutable const void* map_key[4] = {nullptr, nullptr, nullptr, nullptr};
+  mutable bool map_ok = false;
 };
 
 namespace {
@@ -66,7 +73,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsPlan {
   size_t off_pieces, off_chunks, off_f256, off_f128, off_strips, off_tiles, off_muon, off_f32, off_t32, off_bt,
-      off_status, bytes;
+      off_status, off_maps, bytes;
 };
 
 WsPlan ws_plan(const ShardTables& T) {
@@ -94,6 +101,8 @@ WsPlan ws_plan(const ShardTables& T) {
   o = align_up(o + T.band_tiles.size() * sizeof(RegionGroup), 256);
   p.off_status = o;  // device error word, zeroed by the upload
   o += 256;
+  p.off_maps = o;  // 4 tensor maps per map interval, written by the first step on a set of buffers
+  o = align_up(o + T.maps.size() * 4 * kMapBytes, 256);
   p.bytes = o;
   return p;
 }
@@ -158,6 +167,9 @@ int upload_tables(const ShardTables& T, void* dev_ws, size_t ws_bytes, bq_stream
   sh->dev.n_band_tiles = int32_t(T.band_tiles.size());
   sh->dev.max_strip_tiles = T.max_strip_tiles;
   sh->dev.status = reinterpret_cast<int*>(base + p.off_status);
+  sh->dev.tmaps = base + p.off_maps;
+  sh->dev.n_maps = int32_t(T.maps.size());
+  sh->maps = T.maps;
   *out = sh;
   return BQ_OK;
 }
@@ -314,6 +326,41 @@ int bq_pack(const bq_shard* sh, const void* const* grad_ptrs, void* dbuf_grad, f
                      static_cast<uint16_t*>(dbuf_grad), sh->total, scale, accumulate ? 1 : 0, stream);
 }
 
+// The strips' tensor maps for these buffers (grad bf16, master fp32, m, v bytes:
+// 8-row x 256-column boxes of each map interval), or NULL, in which case the
+// strip kernel copies block by block (the same data).  Built and copied into the
+// workspace, on `stream`, when the buffers differ from the last step's; never
+// while the stream is being captured (a captured step with new buffers copies
+// block by block).
+static const void* strip_maps(const bq_shard* sh, const void* grad, const void* master, const void* m,
+                              const void* v, bq_stream_t stream) {
+  if (sh->dev.n_maps == 0) return nullptr;
+  std::lock_guard<std::mutex> lock(sh->map_mu);
+  const void* key[4] = {grad, master, m, v};
+  if (std::equal(key, key + 4, sh->map_key)) return sh->map_ok ? sh->dev.tmaps : nullptr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  constexpr int kElem[4] = {2, 4, 1, 1};
+  std::vector<unsigned char> img(sh->maps.size() * 4 * kMapBytes);
+  bool ok = true;
+  for (size_t i = 0; ok && i < sh->maps.size(); ++i)
+    for (int k = 0; ok && k < 4; ++k) {
+      const MapInterval& mi = sh->maps[i];
+      const auto* base = static_cast<const unsigned char*>(key[k]) + mi.pos * kElem[k];
+      ok = (reinterpret_cast<uintptr_t>(base) & 15) == 0 &&  // tensor map bases are 16-byte aligned
+           encode_map_2d(img.data() + (i * 4 + size_t(k)) * kMapBytes, base, kElem[k], mi.C, mi.rows, 256, 8) == BQ_OK;
+    }
+  if (ok) ok = cudaMemcpyAsync(sh->dev.tmaps, img.data(), img.size(), cudaMemcpyHostToDevice, s) == cudaSuccess;
+  if (!ok) cudaGetLastError();
+  std::copy(key, key + 4, sh->map_key);
+  sh->map_ok = ok;
+  return ok ? sh->dev.tmaps : nullptr;
+}
+
 int bq_step_adam8(const bq_shard* sh, const void* grad, float* master, int8_t* m, uint8_t* v, float* m_scale,
                   float* v_scale, const bq_adam_hp* hp, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream) {
   if (!sh || !grad || !master || !m || !v || !hp) return set_error(BQ_EINVAL, "bq_step_adam8: NULL argument");
@@ -329,7 +376,7 @@ int bq_step_adam8(const bq_shard* sh, const void* grad, float* master, int8_t* m
        reinterpret_cast<uintptr_t>(fp8_scale)) & 3)
     return set_error(BQ_EALIGN, "bq_step_adam8: scale buffers must be 4-byte aligned");
   AdamArgs a{static_cast<const uint16_t*>(grad), master, m, v, m_scale, v_scale, fp8_out, fp8_scale, *hp,
-             sh->dev.status};
+             sh->dev.status, strip_maps(sh, grad, master, m, v, stream)};
   return launch_adam8(sh->dev, a, stream);
 }
 

@@ -68,12 +68,24 @@ struct FlatGroup {
 //    columns (blocks are 256-column row segments, block (r, j) has slot
 //    mslot + r*(C/256) + j); FP8 tile t = columns c0 + 128t, slot fslot + t.
 //  - TILE128 Adam (tile): width <= 128, one tile, Adam slot mslot, FP8 slot fslot.
+//  A 256-column strip also names its interval's 2-D tensor maps: tm (-1: none)
+//  and trow, the strip's first row within that interval.
 struct RegionGroup {
   int64_t pos;
   int32_t rows, C, c0, width;
   int32_t mslot, fslot;
   uint32_t cmul, cshr;  // n / C == umulhi(n, cmul) >> cshr for 0 <= n < 2^31 (cmul 0: C == 1)
+  int32_t tm = -1, trow = 0;
 };
+
+// The rows [0, rows) x C of one 2-D tensor interval that strips cover, from local
+// position pos: the strip kernel reads them through four 2-D tensor maps (grad,
+// master, m, v) built for the caller's buffers, 8 rows x 256 columns a copy.
+struct MapInterval {
+  int64_t pos;
+  int32_t C, rows;
+};
+constexpr int kMapBytes = 128;  // one CUtensorMap
 
 // Division by an invariant integer with a multiply and a shift (Granlund and
 // Montgomery, "Division by invariant integers using multiplication", 1994):
@@ -102,6 +114,7 @@ struct ShardTables {
   std::vector<FlatGroup> flat32;      // TILE32 Adam on 1-D tensors (32-element blocks)
   std::vector<RegionGroup> tiles32;   // TILE32 Adam on 2-D tensors: 32-row band x <= 256 columns
   std::vector<RegionGroup> band_tiles;  // FP8 tiles of FLAT256 tensors with C % 256 != 0 (one group each)
+  std::vector<MapInterval> maps;        // the strips' tensor intervals (4 tensor maps each at step time)
   int64_t nchunks = 0;
   int32_t max_strip_tiles = 0;        // most FP8 column tiles in one strip group
 };
@@ -133,6 +146,8 @@ struct DevTables {
   int32_t n_flat256, n_flat128, n_strips, n_tiles, n_muon, n_flat32, n_tiles32, n_band_tiles;
   int32_t max_strip_tiles;
   int* status;  // device error word: 0, or the site of a wait that timed out
+  void* tmaps;  // 4 tensor maps (grad, master, m, v) per map interval, written before a step uses them
+  int32_t n_maps;
 };
 
 struct AdamArgs {
@@ -145,7 +160,8 @@ struct AdamArgs {
   uint8_t* fp8;      // may be null
   float* fp8_scale;  // may be null
   bq_adam_hp hp;
-  int* status;  // device error word of the shard (set by the launcher)
+  int* status;          // device error word of the shard (set by the launcher)
+  const void* tmaps;    // the strips' tensor maps for these buffers, or NULL (per-block copies)
 };
 
 int launch_pack(const DevTables& t, const uint16_t* const* grads, uint16_t* dst, int64_t total, float scale,
@@ -164,6 +180,9 @@ int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c,
             size_t ws_bytes, void* stream);
 int muon_ns_check(const void* ws, size_t ws_bytes, void* stream);
 int muon_ns_noalloc(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* stream);
+// a 2-D tiled tensor map (no swizzle) over `rows` x `cols` elements of elem_bytes
+// each at base with row pitch cols; boxes of box_cols x box_rows.  map: 128 bytes.
+int encode_map_2d(void* map, const void* base, int elem_bytes, int64_t cols, int64_t rows, int box_cols, int box_rows);
 
 // errors
 int set_error(int code, const std::string& msg);

@@ -1126,6 +1126,22 @@ int muon_ns_workspace(int batch, const bq_mat* mats, size_t* bytes) {
   return BQ_OK;
 }
 
+int encode_map_2d(void* map, const void* base, int elem_bytes, int64_t cols, int64_t rows, int box_cols, int box_rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return BQ_EDEVICE;
+  const CUtensorMapDataType dt = elem_bytes == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(cols) * cuuint64_t(elem_bytes)};
+  const cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(static_cast<CUtensorMap*>(map), dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BQ_OK : BQ_EINVAL;
+}
+
 int muon_ns(int batch, const bq_mat* mats, int steps, float a, float b, float c, float eps, void* ws, size_t ws_bytes,
             void* stream) {
   return run_batch(batch, mats, steps, a, b, c, eps, ws, ws_bytes, stream, true);

@@ -436,9 +436,12 @@ void build_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, ShardTables&
           const int32_t mband = int32_t(mslot + (rb - r0) * C / 256);
           if (C % 256 == 0) {
             // 256-column strips: every Adam block is one row segment of the strip
+            // (C == 256: the strip is its whole band, one flat run; no map needed)
+            if (rb == r0 && C > 256) T.maps.push_back(MapInterval{pos0, int32_t(C), int32_t(r1 - r0)});
             for (int64_t c0 = 0; c0 < C; c0 += 256)
               T.strips.push_back(RegionGroup{bpos + c0, rows, int32_t(C), int32_t(c0), 256,
-                                             int32_t(mband + c0 / 256), int32_t(fband + c0 / 128), cmul, cshr});
+                                             int32_t(mband + c0 / 256), int32_t(fband + c0 / 128), cmul, cshr,
+                                             C > 256 ? int32_t(T.maps.size() - 1) : -1, int32_t(rb - r0)});
             T.max_strip_tiles = std::max(T.max_strip_tiles, 2);
           } else {
             // whole 128-row bands (256-element Adam blocks cross rows): Adam over
@@ -515,7 +518,16 @@ std::string validate_shard_tables(const bq_layout& L, int dev_lo, int dev_hi, co
     if (g.fslot >= 0 && g.width != 256) return "FP8 region that is not a 256-column strip";
     if (g.fslot >= 0 && g.fslot + ceil_div(g.width, 128) > nf) return "strip FP8 slots out of range";
     if (g.fslot >= 0 && ceil_div(g.width, 128) > T.max_strip_tiles) return "strip tile count above the shared-memory bound";
+    if (g.tm >= 0) {  // read through its interval's tensor maps: the box origin must be this strip
+      if (flat || g.tm >= int32_t(T.maps.size())) return "strip map index";
+      const MapInterval& m = T.maps[size_t(g.tm)];
+      if (m.C != g.C || g.trow < 0 || g.trow + g.rows > m.rows || m.pos + int64_t(g.trow) * g.C + g.c0 != g.pos)
+        return "strip outside its map interval";
+    }
   }
+  for (const MapInterval& m : T.maps)
+    if (m.pos < 0 || m.C <= 0 || m.C % 256 || m.rows <= 0 || m.pos + int64_t(m.rows) * m.C > total)
+      return "map interval outside the shard range";
   for (const RegionGroup& g : T.band_tiles) {
     if (g.rows <= 0 || g.rows > 128 || g.width <= 0 || g.width > 128 || g.width % 8 || g.C % 8 || g.pos % 8 ||
         g.pos < 0 || g.c0 + g.width > g.C || (g.width == g.C && g.c0 != 0))
@@ -569,11 +581,17 @@ void append_member_tables(const ShardTables& M, const GroupPlace& at, ShardTable
       dst.push_back(g);
     }
   };
+  const int32_t tm0 = int32_t(G.maps.size());  // the member's map intervals start here
+  for (MapInterval m : M.maps) {
+    m.pos += at.elem;
+    G.maps.push_back(m);
+  }
   auto region = [&](const std::vector<RegionGroup>& src, std::vector<RegionGroup>& dst, bool mslots) {
     for (RegionGroup g : src) {
       g.pos += at.elem;
       if (mslots) g.mslot += int32_t(at.mslot);
       if (g.fslot >= 0) g.fslot += int32_t(at.fslot);
+      if (g.tm >= 0) g.tm += tm0;
       dst.push_back(g);
     }
   };

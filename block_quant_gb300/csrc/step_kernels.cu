@@ -329,6 +329,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) { return
 
 // bulk copy global -> this CTA's shared memory, completion counted on bar
 // (addresses 16-byte aligned, bytes a multiple of 16)
+// rows [y, y + 8) x columns [x, x + 256) of a 2-D tensor map in global memory
+__device__ __forceinline__ void map_load(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];\n" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
                    smem_u32(dst)),
@@ -548,8 +557,10 @@ struct TmaStage {
   uint2 m[kCons][32];   // int8 m codes
   uint2 v[kCons][32];   // uint8 v codes
   float sc[2 * kCons];  // per block: m scale, v scale
+  float pad_[32 - 2 * kCons];
 };
-static_assert(sizeof(TmaStage) % 16 == 0, "stages keep 16-byte alignment");
+static_assert(sizeof(TmaStage) % 128 == 0, "stages keep the 128-byte alignment of tensor copies");
+static_assert(kCons == 8, "a strip stage is one 8-row box of the interval's tensor maps");
 constexpr uint32_t kBlockBytes = 512 + 1024 + 256 + 256;
 
 __device__ __forceinline__ int region_blocks(const RegionGroup& g) {
@@ -589,6 +600,8 @@ __device__ __forceinline__ void strip_producer(const RegionGroup* __restrict__ g
                                                TmaStage* ring, uint64_t* full, uint64_t* empty, int lane) {
   uint32_t k = 0;  // stages issued
   bool ok = true;
+  // tensor copies need 128-byte aligned destinations (the ring's start)
+  const bool maps = a.tmaps != nullptr && (smem_u32(ring) & 127u) == 0;
   for (int gi = ngroups - 1 - int(blockIdx.x); ok && gi >= 0; gi -= int(gridDim.x)) {
     const RegionGroup g = groups[gi];
     const int nblk = region_blocks(g);
@@ -618,6 +631,19 @@ __device__ __forceinline__ void strip_producer(const RegionGroup* __restrict__ g
         else if (lane == 1) bulk_load(S.p[0], a.master + first, 1024 * kCons, &full[s]);
         else if (lane == 2) bulk_load(S.m[0], a.m + first, 256 * kCons, &full[s]);
         else if (lane == 3) bulk_load(S.v[0], a.v + first, 256 * kCons, &full[s]);
+      } else if (maps && g.tm >= 0) {
+        // a strip: rows j .. j + 7 as one 8-row box of each array's tensor map
+        // (rows past the strip arrive too, zero past the interval; nobody reads them)
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], kCons * kBlockBytes);
+        __syncwarp();
+        if (lane < 4) {
+          const unsigned char* mp = static_cast<const unsigned char*>(a.tmaps) + (size_t(g.tm) * 4 + lane) * kMapBytes;
+          void* dst = lane == 0 ? static_cast<void*>(S.g[0])
+                      : lane == 1 ? static_cast<void*>(S.p[0])
+                      : lane == 2 ? static_cast<void*>(S.m[0])
+                                  : static_cast<void*>(S.v[0]);
+          map_load(dst, mp, g.c0, g.trow + j, &full[s]);
+        }
       } else {
         // pass q, lane = 4 w + arr: array arr (g, p, m, v) of the stage's block 8 q + w
         constexpr int kPasses = (kCons + 7) / 8;

@@ -251,7 +251,11 @@ int bq_pack(const bq_shard* shard, const void* const* grad_ptrs, void* dbuf_grad
  * Resources: the 2-D kernels take 64 or 128 tensor-memory columns per CTA for
  * their lifetime (at most 384 of an SM's 512); a CTA whose columns are held by
  * a co-resident kernel (e.g. a tensor-core GEMM on another stream) waits until
- * that kernel's CTA exits. */
+ * that kernel's CTA exits.  The first call on a set of (grad, master, m, v)
+ * buffers writes tensor maps of those buffers into the shard's workspace
+ * (ordered on `stream`; not while the stream is being captured, when the call
+ * reads the same data block by block instead): a shard serves one stream at a
+ * time. */
 int bq_step_adam8(const bq_shard* shard, const void* grad, float* master, int8_t* m, uint8_t* v, float* m_scale,
                   float* v_scale, const bq_adam_hp* hp, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream);
 
