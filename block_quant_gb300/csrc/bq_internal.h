@@ -42,7 +42,7 @@ namespace bq {
 // pack: the destination range of a shard split into chunks of kPackChunk
 // elements; every chunk is covered by consecutive pieces that never cross a
 // chunk boundary.  tensor < 0 marks padding (written as +0).
-constexpr int64_t kPackChunk = 8192;
+constexpr int64_t kPackChunk = 16384;
 struct PackPiece {
   int64_t dst;     // local element position
   int64_t src;     // tensor-flat element offset
