@@ -329,21 +329,21 @@ int bq_pack(const bq_shard* sh, const void* const* grad_ptrs, void* dbuf_grad, f
 // The strips' tensor maps for these buffers (grad bf16, master fp32, m, v bytes:
 // 8-row x 256-column boxes of each map interval), or NULL, in which case the
 // strip kernel copies block by block (the same data).  Built and copied into the
-// workspace, on `stream`, when the buffers differ from the last step's; never
-// while the stream is being captured (a captured step with new buffers copies
-// block by block).
+// workspace, on `stream`, when the buffers differ from the last step's.  A step
+// being captured into a graph never uses them: a replay must not depend on which
+// buffers a later call wrote maps for.
 static const void* strip_maps(const bq_shard* sh, const void* grad, const void* master, const void* m,
                               const void* v, bq_stream_t stream) {
   if (sh->dev.n_maps == 0) return nullptr;
-  std::lock_guard<std::mutex> lock(sh->map_mu);
-  const void* key[4] = {grad, master, m, v};
-  if (std::equal(key, key + 4, sh->map_key)) return sh->map_ok ? sh->dev.tmaps : nullptr;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
     cudaGetLastError();
     return nullptr;
   }
+  std::lock_guard<std::mutex> lock(sh->map_mu);
+  const void* key[4] = {grad, master, m, v};
+  if (std::equal(key, key + 4, sh->map_key)) return sh->map_ok ? sh->dev.tmaps : nullptr;
   constexpr int kElem[4] = {2, 4, 1, 1};
   std::vector<unsigned char> img(sh->maps.size() * 4 * kMapBytes);
   bool ok = true;

@@ -252,10 +252,11 @@ int bq_pack(const bq_shard* shard, const void* const* grad_ptrs, void* dbuf_grad
  * their lifetime (at most 384 of an SM's 512); a CTA whose columns are held by
  * a co-resident kernel (e.g. a tensor-core GEMM on another stream) waits until
  * that kernel's CTA exits.  The first call on a set of (grad, master, m, v)
- * buffers writes tensor maps of those buffers into the shard's workspace
- * (ordered on `stream`; not while the stream is being captured, when the call
- * reads the same data block by block instead): a shard serves one stream at a
- * time. */
+ * buffers writes tensor maps of those buffers into the shard's workspace,
+ * ordered on `stream`, and later calls on the same buffers read through them; a
+ * call made while `stream` is being captured into a graph reads the same data
+ * block by block instead, so a replay never depends on the maps.  A shard
+ * serves one stream at a time. */
 int bq_step_adam8(const bq_shard* shard, const void* grad, float* master, int8_t* m, uint8_t* v, float* m_scale,
                   float* v_scale, const bq_adam_hp* hp, uint8_t* fp8_out, float* fp8_scale, bq_stream_t stream);
 

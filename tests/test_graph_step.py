@@ -2,8 +2,7 @@
 graph gives bit for bit the oracle's result (and what the same calls give
 launched one by one); a second replay equals the oracle's second step.  Covers
 the TMA-fed strip kernel, the 128x128 and 32x32 tile kernels and the flat
-kernels inside a graph, serial and on branches.  The graphed units' shards are
-captured before any eager step on them, so inside the graph the strip kernel
+kernels inside a graph, serial and on branches.  A captured step's strip kernel
 copies block by block, while the eager units' steps read through the tensor
 maps built for their buffers: the two stagings are held to each other and to
 the oracle bit for bit."""
