@@ -6,7 +6,8 @@
 //                  optionally fused with 1x128 FP8 tiles of 1-D tensors
 //   k_strip<FP8>   8-bit Adam with flat 256-element blocks over a 2-D region,
 //                  fused with 128x128 FP8 tiles; inputs staged by a producer
-//                  warp's bulk (TMA) copies, tile amax in shared memory, half
+//                  warp's TMA copies (tensor-map boxes or bulk copies), tile
+//                  amax in shared memory, half
 //                  of each region's updated master kept in tensor memory for
 //                  the FP8 pass
 //   k_tile<FP8>    8-bit Adam with 128x128 state tiles (+ FP8 of the same tile);
@@ -516,9 +517,13 @@ __global__ void __launch_bounds__(kThreads, kAdamCtas) k_flat(const FlatGroup* _
 // are taken by CTAs in a grid-stride loop, last region first (the pack that
 // precedes this step writes the gradient buffer front to back, so its tail is
 // still in L2 when this kernel starts).  Warp kCons is the producer: it fills a
-// ring of kRing shared-memory stages, each with the next kCons Adam blocks (one
-// bulk copy per block and array; the blocks' two scales by cp.async), and runs
-// ahead across region boundaries.  Warps 0..kCons-1 consume one block each per
+// ring of kRing shared-memory stages, each with the next kCons Adam blocks (the
+// blocks' two scales by cp.async), and runs ahead across region boundaries.  A
+// stage takes four copies when it can: a strip's 8 rows as one 8 x 256 box of a
+// 2-D tensor map per array (maps of the caller's buffers, built on the host),
+// a flat piece's 8 consecutive blocks as one bulk copy per array; otherwise
+// one bulk copy per block and array (the copy engine's cost is per copy as
+// much as per byte).  Warps 0..kCons-1 consume one block each per
 // stage: Adam, state and master written back, |p'| folded into per-column-tile
 // maxima in shared memory.  After a region's last stage they compute the tile
 // scales and convert the region's updated master to E4M3: its first 64 rows
