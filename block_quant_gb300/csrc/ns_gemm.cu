@@ -12,7 +12,7 @@
 // A is symmetric, so A A is computed as A A^T (both operands K-major).  They run
 // and store only the tiles touching the upper triangle; a product reading A or B
 // takes each k-block lying below those tiles as the transpose of its stored
-// partner (MN-major TMA boxes and descriptors), so no lower half is ever
+// partner (MN-major TMA copies and descriptors), so no lower half is ever
 // written.  k_gemm_2 runs B X on pairs of CTAs (cta_group::2, 256 x 256 tiles,
 // M = 256 products reading both CTAs' shared memory), X an MN-major operand.
 //
@@ -261,9 +261,10 @@ __device__ __forceinline__ void tile_at(int u, int mt, int nt, int sym, int& m0,
 }
 
 // tmA / tmB: K-major boxes of 64 columns x BM / BN rows.  With a_sym / b_sym,
-// tmAt / tmBt address the same matrices in 64 x 64 boxes for the transposed
-// (MN-major) reads of the k-blocks whose tiles were not stored: a 128-row A box
-// or 256-row B box of one k-block is either stored whole or not at all.
+// tmAt / tmBt are 3-D maps of the same matrices ({64 columns, rows, 64-column
+// chunks}, boxes of 2 / 4 chunks) for the transposed (MN-major) reads of the
+// k-blocks whose tiles were not stored, one copy each: a 128-row A box or
+// 256-row B box of one k-block is either stored whole or not at all.
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_p(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmBt, GemmArgs g) {
@@ -512,10 +513,10 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// D = alpha * (A B) + beta * C with B given as [K x N] N-contiguous (tmB: 64 x 64
-// boxes) and A K-major (tmA: boxes of 64 columns x 128 rows; with a_sym, tmAt's
-// 64 x 64 boxes give the transposed reads of A's k-blocks below its stored
-// tiles).  Pairs walk the 256 x 256 tiles t = cluster, + clusters, ..., row
+// D = alpha * (A B) + beta * C with B given as [K x N] N-contiguous (tmB: a 3-D
+// map of 64-column chunks, two chunks a copy) and A K-major (tmA: boxes of 64
+// columns x 128 rows; with a_sym, tmAt's two-chunk boxes give the transposed
+// reads of A's k-blocks below its stored tiles).  Pairs walk the 256 x 256 tiles t = cluster, + clusters, ..., row
 // blocks fastest.  A pair tile's rows start at a multiple of 256, so its two
 // 128-row halves of a k-block are stored or transposed together and one
 // instruction descriptor serves both.
